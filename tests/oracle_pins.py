@@ -1,0 +1,357 @@
+"""Pins for the fp64 oracle: facts fixed by the mathematics, not by the oracle itself.
+
+Every pin takes ``attn(w, rows=None, probs=False)`` so the same checks run against the real
+oracle and against deliberately broken builds of it (tests/test_oracle_mutants.py).
+"""
+from __future__ import annotations
+
+import json
+import math
+import os
+
+import numpy as np
+import torch
+
+from tiled_attention_gb300 import inputs as I
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+KINDS = ["none", "causal", "sliding", "document", "paged"]
+
+
+def widen(bits):
+    return I.bf16_bits_to_f32(bits).astype(np.float64)
+
+
+def bf16(x):
+    return I.f32_to_bf16_bits(np.asarray(x, dtype=np.float32))
+
+
+def tiny(kind: str, seed: int = 7, window: int = 5):
+    """Small problems with ragged sizes, GQA and several batch entries."""
+    if kind == "none":
+        return I.dense_workload(seed, 2, 4, 2, 37, 16, I.MASK_NONE)
+    if kind == "causal":
+        return I.dense_workload(seed, 2, 4, 2, 37, 16, I.MASK_CAUSAL)
+    if kind == "sliding":
+        return I.dense_workload(seed, 2, 4, 2, 37, 16, I.MASK_SLIDING, window=window)
+    if kind == "document":
+        return I.document_workload(seed, 37, 4, 16, cu_seqlens=[0, 5, 6, 20, 37], Hkv=2)
+    if kind == "paged":
+        return I.paged_decode_workload(seed, 3, 0, 0, 4, 2, 16, page_size=8, spare_pages=3,
+                                       context_lens=[1, 63, 130])
+    raise KeyError(kind)
+
+
+# ---- an independent dense view of each problem, built with torch library routines ----
+
+def dense_problems(w):
+    """Yield (row_index_array, q [R,d], k [L,d], v [L,d], mask [R,L] bool) per (batch, head),
+    with the mask written as whole-matrix torch operations (tril / triu / segment ids)."""
+    qf, kf, vf = widen(w.q), widen(w.k), widen(w.v)
+    group = w.Hq // w.Hkv
+    if w.mask_kind in (I.MASK_NONE, I.MASK_CAUSAL, I.MASK_SLIDING):
+        N = w.N
+        ones = torch.ones(N, N, dtype=torch.bool)
+        if w.mask_kind == I.MASK_NONE:
+            mask = ones
+        elif w.mask_kind == I.MASK_CAUSAL:
+            mask = torch.tril(ones)
+        else:
+            mask = torch.tril(ones) & torch.triu(ones, diagonal=-(w.window - 1))
+        for b in range(w.B):
+            for h in range(w.Hq):
+                rows = (b * w.Hq + h) * N + np.arange(N)
+                yield rows, qf[b, h], kf[b, h // group], vf[b, h // group], mask.numpy()
+    elif w.mask_kind == I.MASK_DOCUMENT:
+        T = w.N
+        seg = torch.bucketize(torch.arange(T), torch.as_tensor(w.cu_seqlens[1:]), right=True)
+        mask = (seg[:, None] == seg[None, :]) & torch.tril(torch.ones(T, T, dtype=torch.bool))
+        for h in range(w.Hq):
+            rows = h * T + np.arange(T)
+            yield rows, qf[0, h], kf[0, h // group], vf[0, h // group], mask.numpy()
+    else:
+        P = w.page_size
+        for b in range(w.B):
+            L = int(w.cu_seqlens[b + 1] - w.cu_seqlens[b])
+            pages = [int(w.block_table[b, p]) for p in range((L + P - 1) // P)]
+            for h in range(w.Hq):
+                g = h // group
+                kk = np.concatenate([kf[p, g] for p in pages], axis=0)[:L] if L else np.zeros((0, w.d))
+                vv = np.concatenate([vf[p, g] for p in pages], axis=0)[:L] if L else np.zeros((0, w.d))
+                yield (np.array([b * w.Hq + h]), qf[b, h], kk, vv, np.ones((1, L), dtype=bool))
+
+
+def brute_force(w):
+    """softmax(scale * Q K^T with masked entries -inf) @ V and logsumexp, torch fp64."""
+    n = int(np.prod(w.lse_shape))
+    O = np.zeros((n, w.d))
+    L = np.zeros(n)
+    s = float(np.float32(w.scale))
+    for rows, q, k, v, mask in dense_problems(w):
+        z = s * (torch.as_tensor(q) @ torch.as_tensor(k).T)
+        z = z.masked_fill(~torch.as_tensor(mask), float("-inf"))
+        O[rows] = (torch.softmax(z, dim=-1) @ torch.as_tensor(v)).numpy()
+        L[rows] = torch.logsumexp(z, dim=-1).numpy()
+    return O, L
+
+
+def visible_lists(w):
+    out = {}
+    for rows, q, k, v, mask in dense_problems(w):
+        for t, r in enumerate(rows):
+            out[int(r)] = (np.nonzero(mask[t])[0], v, k, q[t])
+    return out
+
+
+# ---------------------------------- pins ----------------------------------
+
+def pin_brute_force(attn, kind):
+    w = tiny(kind)
+    o, lse = attn(w)
+    bo, bl = brute_force(w)
+    np.testing.assert_allclose(o, bo, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, bl, rtol=0, atol=1e-12)
+
+
+def pin_q_zero_mean(attn, kind):
+    """Q = 0: every visible score is 0, so O is the plain mean of the visible V rows and
+    LSE = ln |V(i)|."""
+    w = tiny(kind)
+    w.q[...] = 0
+    o, lse = attn(w)
+    for r, (vis, v, _, _) in visible_lists(w).items():
+        np.testing.assert_allclose(o[r], v[vis].mean(axis=0), rtol=0, atol=1e-13)
+        assert abs(lse[r] - math.log(len(vis))) < 1e-13
+
+
+def pin_dominant_logit(attn, kind):
+    """One key scoring 256 above every other visible key selects its V row."""
+    base = tiny(kind)
+    vis = visible_lists(base)
+    for r in sorted(vis)[:: max(1, len(vis) // 9)]:
+        w = tiny(kind)
+        idx, _, _, _ = vis[r]
+        jstar = int(idx[len(idx) // 2])
+        _set_dominant(w, r, jstar)
+        o, _ = attn(w, rows=np.array([r]))
+        vrow = visible_lists(w)[r][1][jstar]
+        np.testing.assert_allclose(o[0], vrow, rtol=0, atol=1e-12)
+
+
+def _set_dominant(w, r, jstar):
+    """Query row r and key j* get component 0 equal to 32; every other key of that head gets
+    component 0 equal to 0 and the query's other components are 0. Then z(r, j*) = 1024*s and
+    every other visible score is 0."""
+    group = w.Hq // w.Hkv
+    if w.mask_kind == I.MASK_PAGED_DECODE:
+        b, h = divmod(r, w.Hq)
+        g = h // group
+        w.q[b, h, 0, :] = 0
+        w.q[b, h, 0, 0] = bf16(32.0)
+        w.k[:, g, :, 0] = 0
+        P = w.page_size
+        w.k[w.block_table[b, jstar // P], g, jstar % P, 0] = bf16(32.0)
+        return
+    if w.mask_kind == I.MASK_DOCUMENT:
+        h, i = divmod(r, w.N)
+        b = 0
+    else:
+        b, rem = divmod(r, w.Hq * w.N)
+        h, i = divmod(rem, w.N)
+    g = h // group
+    w.q[b, h, i, :] = 0
+    w.q[b, h, i, 0] = bf16(32.0)
+    w.k[b, g, :, 0] = 0
+    w.k[b, g, jstar, 0] = bf16(32.0)
+
+
+def pin_probabilities(attn, kind):
+    """Each softmax row is non-negative, sums to 1 and is zero off the visible set."""
+    w = tiny(kind)
+    _, _, p = attn(w, probs=True)
+    for r, (vis, _, _, _) in visible_lists(w).items():
+        row = p[r]
+        assert np.all(row >= 0)
+        assert abs(row.sum() - 1.0) < 1e-13
+        off = np.ones(row.size, dtype=bool)
+        off[vis] = False
+        assert np.all(row[off] == 0)
+
+
+def pin_single_key_rows(attn, kind):
+    """A row that sees exactly one key returns that key's V row exactly and LSE = its score."""
+    if kind == "sliding":
+        w = tiny(kind, window=1)
+    elif kind == "none":
+        w = I.dense_workload(5, 2, 4, 2, 1, 16, I.MASK_NONE)
+    else:
+        w = tiny(kind)
+    o, lse = attn(w)
+    s = float(np.float32(w.scale))
+    seen = 0
+    for r, (vis, v, k, q) in visible_lists(w).items():
+        if len(vis) != 1:
+            continue
+        j = int(vis[0])
+        assert np.array_equal(o[r], v[j])
+        assert abs(lse[r] - s * float(np.dot(q, k[j]))) < 1e-12
+        seen += 1
+    assert seen > 0
+
+
+def pin_constant_values(attn, kind):
+    """V identically c gives O = c for every row."""
+    w = tiny(kind)
+    c = 0.3671875
+    w.v[...] = bf16(c)
+    o, _ = attn(w)
+    np.testing.assert_allclose(o, c, rtol=0, atol=1e-14)
+
+
+def pin_logit_shift(attn, kind):
+    """Adding the same constant to every score of a row changes LSE by that constant and
+    leaves O unchanged (done through a component that is 1 in every key)."""
+    w0 = tiny(kind)
+    if kind == "paged":
+        w0.k[:, :, :, 0] = bf16(1.0)
+        w0.q[:, :, :, 0] = 0
+    else:
+        w0.k[..., 0] = bf16(1.0)
+        w0.q[..., 0] = 0
+    w1 = tiny(kind)
+    w1.k[...] = w0.k
+    w1.q[...] = w0.q
+    w1.q[..., 0] = bf16(5.0)
+    o0, l0 = attn(w0)
+    o1, l1 = attn(w1)
+    s = float(np.float32(w0.scale))
+    np.testing.assert_allclose(o1, o0, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(l1 - l0, 5.0 * s, rtol=0, atol=1e-12)
+
+
+def pin_key_permutation(attn):
+    """Without a mask, reordering keys and values together changes nothing."""
+    w = tiny("none")
+    perm = np.random.default_rng(3).permutation(w.N)
+    wp = tiny("none")
+    wp.k[...] = w.k[:, :, perm]
+    wp.v[...] = w.v[:, :, perm]
+    o0, l0 = attn(w)
+    o1, l1 = attn(wp)
+    np.testing.assert_allclose(o1, o0, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(l1, l0, rtol=0, atol=1e-12)
+
+
+def pin_window_covering_equals_causal(attn):
+    c = tiny("causal")
+    for W in (c.N, c.N + 1, 10 * c.N):
+        s = tiny("sliding", window=W)
+        assert np.array_equal(attn(s)[0], attn(c)[0])
+        assert np.array_equal(attn(s)[1], attn(c)[1])
+    s = tiny("sliding", window=c.N - 1)
+    assert not np.array_equal(attn(s)[0], attn(c)[0])
+
+
+def pin_single_segment_equals_causal(attn):
+    c = I.dense_workload(11, 1, 4, 2, 37, 16, I.MASK_CAUSAL)
+    d = I.document_workload(11, 37, 4, 16, cu_seqlens=[0, 37], Hkv=2)
+    d.q[...], d.k[...], d.v[...] = c.q, c.k, c.v
+    assert np.array_equal(attn(d)[0], attn(c)[0])
+    assert np.array_equal(attn(d)[1], attn(c)[1])
+
+
+def pin_gqa_equals_repeated_mha(attn, kind):
+    w = tiny(kind)
+    group = w.Hq // w.Hkv
+    if kind == "paged":
+        m = I.paged_decode_workload(7, 3, 0, 0, 4, 4, 16, page_size=8, spare_pages=3,
+                                    context_lens=[1, 63, 130])
+        m.block_table = w.block_table.copy()
+    elif kind == "document":
+        m = I.document_workload(7, 37, 4, 16, cu_seqlens=[0, 5, 6, 20, 37], Hkv=4)
+    else:
+        m = I.dense_workload(7, 2, 4, 4, 37, 16, w.mask_kind, window=w.window)
+    m.q[...] = w.q
+    m.k[...] = np.repeat(w.k, group, axis=1)
+    m.v[...] = np.repeat(w.v, group, axis=1)
+    assert np.array_equal(attn(m)[0], attn(w)[0])
+    assert np.array_equal(attn(m)[1], attn(w)[1])
+
+
+def pin_paged_equals_dense_last_row(attn):
+    """Decode of sequence b equals the last row of causal attention over its L_b tokens laid
+    out contiguously (the query is the last token and sees the whole context)."""
+    w = tiny("paged")
+    o, lse = attn(w)
+    P = w.page_size
+    for b in range(w.B):
+        L = int(w.cu_seqlens[b + 1] - w.cu_seqlens[b])
+        pages = [int(w.block_table[b, p]) for p in range((L + P - 1) // P)]
+        dk = np.concatenate([w.k[p] for p in pages], axis=1)[:, :L]
+        dv = np.concatenate([w.v[p] for p in pages], axis=1)[:, :L]
+        dn = I.dense_workload(0, 1, w.Hq, w.Hkv, L, w.d, I.MASK_CAUSAL)
+        dn.k[0], dn.v[0] = dk, dv
+        dn.q[0, :, L - 1] = w.q[b, :, 0]
+        rows = np.arange(w.Hq) * L + (L - 1)
+        od, ld = attn(dn, rows=rows)
+        assert np.array_equal(od, o[b * w.Hq:(b + 1) * w.Hq])
+        assert np.array_equal(ld, lse[b * w.Hq:(b + 1) * w.Hq])
+
+
+def pin_online_recurrence(attn, kind):
+    """The running-max / running-sum update over key tiles (m_new = max(m, tile max),
+    rescale by exp(m - m_new), l = alpha*l + sum p, acc = alpha*acc + p v; divide by l at
+    the end) gives the same function as the two-pass oracle, for any tile width."""
+    w = tiny(kind)
+    o, lse = attn(w)
+    s = float(np.float32(w.scale))
+    for tile in (1, 3, 16, 64):
+        for rows, q, k, v, mask in dense_problems(w):
+            z = s * (q @ k.T)
+            z = np.where(mask, z, -np.inf)
+            R = z.shape[0]
+            m = np.full(R, -np.inf)
+            l = np.zeros(R)
+            acc = np.zeros((R, w.d))
+            for j0 in range(0, z.shape[1], tile):
+                st = z[:, j0:j0 + tile]
+                m_new = np.maximum(m, st.max(axis=1))
+                safe = np.where(np.isinf(m_new), 0.0, m_new)
+                alpha = np.exp(m - safe)
+                p = np.exp(st - safe[:, None])
+                l = alpha * l + p.sum(axis=1)
+                acc = alpha[:, None] * acc + p @ v[j0:j0 + tile]
+                m = m_new
+            np.testing.assert_allclose(acc / l[:, None], o[rows], rtol=0, atol=1e-12)
+            np.testing.assert_allclose(m + np.log(l), lse[rows], rtol=0, atol=1e-12)
+
+
+def pin_closed_form_golden(attn):
+    g = json.load(open(os.path.join(GOLDEN, "closed_form_2x2.json")))
+    inp = g["inputs"]
+    kinds = {"none": I.MASK_NONE, "causal": I.MASK_CAUSAL, "sliding": I.MASK_SLIDING}
+    for case in g["cases"]:
+        w = I.dense_workload(0, 1, 1, 1, 2, 2, kinds[case["mask"]], window=case["window"])
+        w.scale = inp["scale"]
+        w.q[0, 0] = bf16(inp["q"])
+        w.k[0, 0] = bf16(inp["k"])
+        w.v[0, 0] = bf16(inp["v"])
+        o, lse = attn(w)
+        np.testing.assert_allclose(o, np.array(case["o"]), rtol=0, atol=1e-15)
+        np.testing.assert_allclose(lse, np.array(case["lse"]), rtol=0, atol=1e-15)
+
+
+def all_pins():
+    """(name, callable(attn)) for every pin, each kind where it applies."""
+    pins = []
+    for kind in KINDS:
+        for f in (pin_brute_force, pin_q_zero_mean, pin_dominant_logit, pin_probabilities,
+                  pin_single_key_rows, pin_constant_values, pin_logit_shift,
+                  pin_gqa_equals_repeated_mha, pin_online_recurrence):
+            pins.append((f"{f.__name__}[{kind}]", (lambda f, kind: lambda a: f(a, kind))(f, kind)))
+    for f in (pin_key_permutation, pin_window_covering_equals_causal,
+              pin_single_segment_equals_causal, pin_paged_equals_dense_last_row,
+              pin_closed_form_golden):
+        pins.append((f.__name__, f))
+    return pins
