@@ -1,0 +1,159 @@
+/*
+ * attn.h — C ABI of the GB300 (sm_103a) tiled attention forward library (libtiled_attn.so).
+ *
+ * The library computes O = softmax(scale * Q K^T + mask) V without materialising the score
+ * matrix: each query tile keeps a running row max m and row sum l and rescales its
+ * accumulator by exp(m - m_new) when the max grows ("Flash MSA Attention Kernel
+ * Implementation Tutorial", section "Understanding Flash MSA Core Mechanics"). It also returns
+ * the natural-log log-sum-exp of the scaled, masked scores of every query row.
+ *
+ * Conventions shared by every entry point:
+ *  - All tensor pointers are DEVICE pointers owned by the caller. The library never allocates,
+ *    frees or retains them beyond the call. Elements are bf16 (raw 16-bit patterns) unless
+ *    stated; LSE is fp32. Every tensor is contiguous and 16-byte aligned.
+ *  - Calls are asynchronous on the given stream (a cudaStream_t; NULL = legacy default stream)
+ *    and never synchronise the host, except attn_get_status().
+ *  - Errors are returned, never thrown or printed: 0 on success, a negative ATTN_ERR_* code
+ *    otherwise, with a message for attn_last_error(). An invalid call launches nothing.
+ *  - Conditions only the device can see (a bad cu_seqlens entry, a block-table entry outside
+ *    the pool, a pipeline wait that ran past its time limit) are written to a device status
+ *    word that attn_get_status() reads and clears.
+ */
+#ifndef TILED_ATTN_H
+#define TILED_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Which keys a query row i may attend to (j indexes keys):
+ *  NONE          every key j < N.
+ *  CAUSAL        j <= i.
+ *  SLIDING       i - window < j <= i (causal window of `window` keys, the query included;
+ *                "Optimizing Triton Kernels for Custom Attention Patterns on H100",
+ *                Pattern B, read as a causal window).
+ *  DOCUMENT      cu_seqlens[s] <= j <= i where segment s holds i (no attention across
+ *                segments, causal inside one; same page, Pattern A).
+ *  PAGED_DECODE  one query per sequence sees its whole context, read through a block table
+ *                (same page, Pattern C). */
+enum attn_mask_kind {
+    ATTN_MASK_NONE = 0,
+    ATTN_MASK_CAUSAL = 1,
+    ATTN_MASK_SLIDING = 2,
+    ATTN_MASK_DOCUMENT = 3,
+    ATTN_MASK_PAGED_DECODE = 4
+};
+
+enum attn_status {
+    ATTN_OK = 0,
+    ATTN_ERR_INVALID = -1,     /* an argument breaks the contract below */
+    ATTN_ERR_UNSUPPORTED = -2, /* valid attention, but outside what the kernels implement */
+    ATTN_ERR_CUDA = -3,        /* a CUDA runtime / driver call failed */
+    ATTN_ERR_TIMEOUT = -4,     /* (status word) a pipeline wait gave up after its time limit */
+    ATTN_ERR_BOUNDS = -5,      /* (status word) block-table entry outside [0, num_pages) */
+    ATTN_ERR_WORKSPACE = -6,   /* workspace missing or smaller than attn_workspace_bytes() */
+    ATTN_ERR_SEQLENS = -7      /* (status word) cu_seqlens not monotone / not ending at N */
+};
+
+/*
+ * attn_fwd — fused tiled attention forward pass.
+ *
+ * q, o      bf16. Dense kinds [B,Hq,N,d]; DOCUMENT [1,Hq,N,d] with N = total packed tokens;
+ *           PAGED_DECODE [B,Hq,1,d].
+ * k, v      bf16. Dense kinds [B,Hkv,N,d]; DOCUMENT [1,Hkv,N,d]; PAGED_DECODE page pools
+ *           [num_pages,Hkv,page_size,d] (one (page, kv-head) block is contiguous).
+ * lse       fp32, ln sum_j exp(scale * q_i . k_j) over the visible keys. [B,Hq,N]; DOCUMENT
+ *           [1,Hq,N]; PAGED_DECODE [B,Hq].
+ * B         batch (dense), number of segments (DOCUMENT) or sequences (PAGED_DECODE).
+ * Hq, Hkv   query / key-value heads; Hq % Hkv == 0; query head h reads kv head h/(Hq/Hkv).
+ * N         keys per sequence (dense), packed tokens (DOCUMENT), or the longest context
+ *           (PAGED_DECODE: block_table has ceil(N/page_size) columns).
+ * d         head dimension; 64 or 128 (else ATTN_ERR_UNSUPPORTED).
+ * scale     multiplies q.k before the softmax (callers usually pass 1/sqrt(d)).
+ * mask_kind enum attn_mask_kind.
+ * window    SLIDING only: number of keys visible to a query (>= 1). Ignored otherwise.
+ * cu_seqlens int32 device array [B+1], cu[0] = 0, nondecreasing. DOCUMENT: segment starts,
+ *           cu[B] = N. PAGED_DECODE: cumulative context lengths (L_b = cu[b+1] - cu[b],
+ *           0 <= L_b <= N). Checked on the device (status ATTN_ERR_SEQLENS). Unused otherwise.
+ * block_table int32 device array [B, ceil(N/page_size)]: physical page of logical page p of
+ *           sequence b; entries past a sequence's last page are ignored (-1 by convention).
+ *           PAGED_DECODE only.
+ * page_size tokens per page; PAGED_DECODE supports 64.
+ * num_pages pages in the k / v pools (PAGED_DECODE; bounds-checked on the device).
+ * workspace device scratch of at least attn_workspace_bytes(...) bytes (may be NULL when that
+ *           is 0). Its contents need not be initialised; concurrent calls need separate ones.
+ * stream    cudaStream_t to launch on.
+ * A sequence with L_b = 0 gets O = 0 and LSE = -inf.
+ */
+int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq,
+             int Hkv, int N, int d, float scale, int mask_kind, int window,
+             const int32_t *cu_seqlens, const int32_t *block_table, int page_size,
+             int num_pages, void *workspace, size_t workspace_bytes, void *stream);
+
+/* Bytes of workspace attn_fwd needs for these arguments (0 for the prefill kinds). */
+size_t attn_workspace_bytes(int B, int Hq, int Hkv, int N, int d, int mask_kind, int page_size);
+
+/*
+ * attn_gather_pages — copy paged K or V into a dense per-sequence layout.
+ * pool [num_pages,Hkv,page_size,d] bf16 -> dst [B,Hkv,max_pages*page_size,d] bf16 where
+ * dst[b,g,p*page_size + t] = pool[block_table[b,p], g, t]. Pages whose table entry is negative
+ * are left untouched. Entries >= num_pages set ATTN_ERR_BOUNDS in the status word and are
+ * skipped. This is the page-gather stage of the two-stage paged path of "Optimizing Triton
+ * Kernels for Custom Attention Patterns on H100", Pattern C; the fused decode reads pages
+ * in place instead.
+ */
+int attn_gather_pages(const void *pool, void *dst, const int32_t *block_table, int B,
+                      int max_pages, int Hkv, int page_size, int d, int num_pages,
+                      void *stream);
+
+/* Synchronises `stream`, then returns and clears the device status word (ATTN_OK or one of
+ * ATTN_ERR_TIMEOUT / ATTN_ERR_BOUNDS / ATTN_ERR_SEQLENS), or ATTN_ERR_CUDA if the stream
+ * reported a CUDA error. */
+int attn_get_status(void *stream);
+
+/* Message for the last non-zero return on the calling thread ("" if none). Thread-local;
+ * valid until the next call on that thread. */
+const char *attn_last_error(void);
+
+/* Frees the library's cached device state (status word) on the current device. */
+void attn_release(void);
+
+/* Library version, (major << 16) | minor. */
+int attn_version(void);
+
+/*
+ * Host-only planning helpers (no CUDA calls; usable without a GPU). They run the same
+ * tile-classification code the kernels run, so tests can check the schedule exhaustively.
+ *
+ * attn_plan_kv_range: for query rows [r0, min(r0+bm, row_end)) and keys indexed from k_org
+ * (valid keys [k_org, k_end)), the half-open range [*lo, *hi) of bn-wide key tiles (tile t
+ * covers keys k_org + t*bn ... + bn-1) holding at least one visible pair. *hi <= *lo when
+ * none does. Returns 0, or ATTN_ERR_INVALID.
+ *
+ * attn_plan_tile_kind: 0 if tile t holds no visible pair for those rows, 1 if every (row,
+ * key) pair in it is visible (no element mask needed), 2 if it is a boundary tile.
+ */
+int attn_plan_kv_range(int mask_kind, int window, int r0, int bm, int row_end, int k_org,
+                       int k_end, int bn, int *lo, int *hi);
+int attn_plan_tile_kind(int mask_kind, int window, int r0, int bm, int row_end, int k_org,
+                        int k_end, int bn, int t);
+
+/*
+ * attn_plan_units: the prefill work list in launch order. One unit is a pair of bm-row query
+ * tiles of one (batch or segment, query head); units are ordered longest-first (pair index
+ * descending), then by batch/segment, then head, so the heaviest causal tiles start first and
+ * heads sharing a kv head run side by side. cu_seqlens is a HOST array here (DOCUMENT only).
+ * Writes up to max_units records of 3 ints (segment or batch, head, pair index) to out and
+ * returns the unit count (or a negative ATTN_ERR_*).
+ */
+int attn_plan_units(int mask_kind, int B, int Hq, int N, const int32_t *cu_seqlens_host,
+                    int32_t *out, int max_units);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TILED_ATTN_H */

@@ -1,0 +1,179 @@
+"""C-ABI library checks that need no GPU: it builds for sm_103a, loads, exports every symbol
+include/attn.h declares, rejects bad arguments before touching CUDA, and its tile scheduler is
+exact (checked exhaustively against the mask definitions on small tiles)."""
+import itertools
+
+import numpy as np
+import pytest
+
+from tiled_attention_gb300 import attn, build
+
+NONE, CAUSAL, SLIDING, DOCUMENT = 0, 1, 2, 3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def library():
+    build.build()
+    return attn.lib()
+
+
+def test_exports_every_declared_symbol():
+    names = attn.declared_functions()
+    assert len(names) >= 10
+    L = attn.lib()
+    for n in names:
+        assert hasattr(L, n), n
+    assert set(names) == set(attn._SIGS), "binding and header disagree"
+
+
+def test_version():
+    assert attn.attn_version() == 1
+
+
+def _call(**kw):
+    a = dict(q=None, k=None, v=None, o=None, lse=None, B=1, Hq=1, Hkv=1, N=128, d=128,
+             scale=0.125, mask_kind=CAUSAL, window=0, cu_seqlens=None, block_table=None,
+             page_size=0, num_pages=0, workspace=None, stream=0)
+    a.update(kw)
+    return attn.attn_fwd(**a)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(mask_kind=7), attn.ATTN_ERR_INVALID),
+    (dict(Hq=6, Hkv=4), attn.ATTN_ERR_INVALID),
+    (dict(d=96), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(d=256), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(scale=float("nan")), attn.ATTN_ERR_INVALID),
+    (dict(scale=-1.0), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(mask_kind=SLIDING, window=0), attn.ATTN_ERR_INVALID),
+    (dict(mask_kind=DOCUMENT), attn.ATTN_ERR_INVALID),
+    (dict(B=-1), attn.ATTN_ERR_INVALID),
+    (dict(Hkv=0), attn.ATTN_ERR_INVALID),
+])
+def test_invalid_arguments_are_rejected_without_cuda(kw, code):
+    assert _call(**kw) == code
+    assert attn.last_error()
+
+
+def test_empty_problem_is_a_no_op():
+    assert _call(B=0) == attn.ATTN_OK
+    assert _call(N=0) == attn.ATTN_OK
+
+
+def test_null_tensors_rejected():
+    assert _call() == attn.ATTN_ERR_INVALID
+
+
+def test_workspace_bytes():
+    assert attn.attn_workspace_bytes(4, 16, 16, 2048, 128, CAUSAL, 0) == 0
+    n = attn.attn_workspace_bytes(32, 32, 8, 16384, 128, 4, 64)
+    # partial O for 16 splits x 4 heads x 128 columns per (sequence, kv head), plus stats
+    assert n >= 32 * 8 * 16 * 4 * 128 * 4
+
+
+# ---------------------------------------------------------------- tile scheduler
+
+def visible(mask, W, k_org, k_end, i, j):
+    """Key j visible to query row i (keys and rows share one index space)."""
+    if j < k_org or j >= k_end:
+        return False
+    if mask == NONE:
+        return True
+    if mask == CAUSAL or mask == DOCUMENT:
+        return j <= i
+    return i - W < j <= i
+
+
+def check_schedule(mask, W, r0, bm, row_end, k_org, k_end, bn):
+    lo, hi = attn.attn_plan_kv_range(mask, W, r0, bm, row_end, k_org, k_end, bn)
+    rows = range(r0, min(r0 + bm, row_end))
+    ntiles = (k_end - k_org + bn - 1) // bn + 2
+    nonempty = []
+    for t in range(-1, ntiles):
+        keys = range(k_org + t * bn, k_org + (t + 1) * bn)
+        vis = [[visible(mask, W, k_org, k_end, i, j) for j in keys] for i in rows]
+        anyv = any(any(r) for r in vis)
+        allv = len(rows) > 0 and all(all(r) for r in vis)
+        if t >= 0:
+            kind = attn.attn_plan_tile_kind(mask, W, r0, bm, row_end, k_org, k_end, bn, t)
+            want = 0 if not anyv else (1 if allv else 2)
+            assert kind == want, (mask, W, r0, bm, row_end, k_org, k_end, bn, t, kind, want)
+        if anyv:
+            nonempty.append(t)
+    if nonempty:
+        assert (lo, hi) == (min(nonempty), max(nonempty) + 1)
+        assert nonempty == list(range(lo, hi)), "visible tiles must be contiguous"
+    else:
+        assert hi <= lo
+
+
+@pytest.mark.parametrize("bm,bn", [(4, 4), (4, 8), (8, 4), (3, 5)])
+def test_schedule_dense_exhaustive(bm, bn):
+    for N in range(1, 23):
+        for r0 in range(0, N, bm):
+            check_schedule(NONE, 0, r0, bm, N, 0, N, bn)
+            check_schedule(CAUSAL, 0, r0, bm, N, 0, N, bn)
+            for W in (1, 2, 3, 4, 5, 7, 8, 9, N, N + 3):
+                check_schedule(SLIDING, W, r0, bm, N, 0, N, bn)
+
+
+@pytest.mark.parametrize("bm,bn", [(4, 4), (4, 8), (8, 4)])
+def test_schedule_document_exhaustive(bm, bn):
+    cu = [0, 1, 3, 8, 9, 17, 30]
+    for s in range(len(cu) - 1):
+        for r0 in range(cu[s], cu[s + 1], bm):
+            check_schedule(DOCUMENT, 0, r0, bm, cu[s + 1], cu[s], cu[s + 1], bn)
+
+
+def test_schedule_kernel_tile_sizes():
+    """128 x 128 tiles (the kernels' sizes) on ragged sizes, spot-checked per tile."""
+    for N in (1, 127, 128, 129, 300):
+        for r0 in range(0, N, 128):
+            check_schedule(CAUSAL, 0, r0, 128, N, 0, N, 128)
+            check_schedule(NONE, 0, r0, 128, N, 0, N, 128)
+            for W in (1, 127, 128, 129, 200):
+                check_schedule(SLIDING, W, r0, 128, N, 0, N, 128)
+
+
+def test_schedule_skips_masked_tiles():
+    """Causal N=2048: 8 query-tile pairs; tile row r sees r+1 key tiles, one boundary."""
+    total = 0
+    for r in range(16):
+        lo, hi = attn.attn_plan_kv_range(CAUSAL, 0, 128 * r, 128, 2048, 0, 2048, 128)
+        assert (lo, hi) == (0, r + 1)
+        kinds = [attn.attn_plan_tile_kind(CAUSAL, 0, 128 * r, 128, 2048, 0, 2048, 128, t)
+                 for t in range(16)]
+        assert kinds == [1] * r + [2] + [0] * (15 - r)
+        total += hi - lo
+    assert total == 136
+    # Sliding window 4096 at N=8192: at most 33 key tiles, at most 2 boundary tiles.
+    for r in range(64):
+        lo, hi = attn.attn_plan_kv_range(SLIDING, 4096, 128 * r, 128, 8192, 0, 8192, 128)
+        kinds = [attn.attn_plan_tile_kind(SLIDING, 4096, 128 * r, 128, 8192, 0, 8192, 128, t)
+                 for t in range(lo, hi)]
+        assert hi - lo <= 33 and kinds.count(2) <= 2 and 0 not in kinds
+
+
+def test_units_dense_order_and_cover():
+    B, Hq, N = 2, 3, 700
+    u = attn.attn_plan_units(CAUSAL, B, Hq, N)
+    npairs = (N + 255) // 256
+    assert len(u) == B * Hq * npairs
+    assert sorted(u) == sorted(itertools.product(range(B), range(Hq), range(npairs)))
+    levels = [t for _, _, t in u]
+    assert levels == sorted(levels, reverse=True)
+
+
+def test_units_document_order_and_cover():
+    cu = np.array([0, 5, 600, 601, 1400, 1400, 1700], dtype=np.int32)
+    Hq = 2
+    u = attn.attn_plan_units(DOCUMENT, len(cu) - 1, Hq, int(cu[-1]), cu)
+    want = [(s, h, t) for s in range(len(cu) - 1) for h in range(Hq)
+            for t in range((int(cu[s + 1] - cu[s]) + 255) // 256)]
+    assert sorted(u) == sorted(want)
+    levels = [t for _, _, t in u]
+    assert levels == sorted(levels, reverse=True)
+    # within a level: segments ascending, then heads
+    for t in set(levels):
+        same = [(s, h) for s, h, tt in u if tt == t]
+        assert same == sorted(same)

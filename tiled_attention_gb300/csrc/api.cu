@@ -1,0 +1,388 @@
+// api.cu — the C ABI of include/attn.h: argument validation, tensor-map encoding, work-list
+// sizing, kernel dispatch, the device status word, the page-gather kernel and the host-side
+// planning helpers.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "../../include/attn.h"
+#include "launch.h"
+#include "sched.h"
+
+namespace ta {
+
+// ------------------------------------------------------------------ errors
+namespace {
+thread_local std::string g_last_error;
+
+int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(ATTN_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+}  // namespace
+
+// ------------------------------------------------------------------ device status word
+// One int per device (a __device__ variable exists once per device context).
+__device__ int g_status_word;
+
+namespace {
+constexpr int kMaxDevices = 64;
+int* g_status_ptr[kMaxDevices];
+std::mutex g_mu;
+
+int status_ptr(int** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(ATTN_ERR_UNSUPPORTED, "device %d", dev);
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_status_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_status_word);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(status)");
+    g_status_ptr[dev] = static_cast<int*>(p);
+  }
+  *out = g_status_ptr[dev];
+  return ATTN_OK;
+}
+
+// ------------------------------------------------------------------ tensor maps
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+int get_encoder(PFN_cuTensorMapEncodeTiled_v12000* fn) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_encode) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                                     cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !p)
+      return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  *fn = g_encode;
+  return ATTN_OK;
+}
+
+// 3-D bf16 view [planes][rows][inner] with a 64-column x box_rows box, 128-byte swizzle.
+int encode_3d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint64_t planes,
+              uint32_t box_rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc;
+  int rc = get_encoder(&enc);
+  if (rc) return rc;
+  cuuint64_t dims[3] = {inner, rows, planes};
+  cuuint64_t strides[2] = {inner * 2, inner * 2 * rows};
+  cuuint32_t box[3] = {64, box_rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return ATTN_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+constexpr unsigned long long kTimeoutNs = 2000000000ull;  // 2 s per pipeline wait
+constexpr int kDecodeChunkPages = 16;
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct DecodeLayout {
+  size_t part_o, part_ml, counters, total;
+  int max_pages, max_splits;
+};
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+DecodeLayout decode_layout(int B, int Hq, int Hkv, int N, int d, int page_size) {
+  DecodeLayout L{};
+  L.max_pages = (N + page_size - 1) / page_size;
+  L.max_splits = (L.max_pages + kDecodeChunkPages - 1) / kDecodeChunkPages;
+  const size_t groups = static_cast<size_t>(B) * Hkv;
+  const size_t G = Hkv > 0 ? static_cast<size_t>(Hq / Hkv) : 0;
+  L.part_o = 0;
+  L.part_ml = align256(groups * L.max_splits * G * d * sizeof(float));
+  L.counters = L.part_ml + align256(groups * L.max_splits * G * 2 * sizeof(float));
+  L.total = L.counters + align256(groups * sizeof(int));
+  return L;
+}
+}  // namespace
+
+cudaError_t ensure_smem_attr(const void* func, int bytes, unsigned long long* done_mask) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = 1ull << (dev & 63);
+  if (__atomic_load_n(done_mask, __ATOMIC_ACQUIRE) & bit) return cudaSuccess;
+  e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) __atomic_fetch_or(done_mask, bit, __ATOMIC_RELEASE);
+  return e;
+}
+
+// ------------------------------------------------------------------ page gather
+__global__ void gather_pages_kernel(const uint4* __restrict__ pool, uint4* __restrict__ dst,
+                                    const int* __restrict__ table, int max_pages, int Hkv,
+                                    int page_vec, int num_pages, int* status) {
+  const int p = static_cast<int>(blockIdx.x);
+  const int b = static_cast<int>(blockIdx.y);
+  const int phys = table[static_cast<size_t>(b) * max_pages + p];
+  if (phys < 0) return;
+  if (phys >= num_pages) {
+    if (threadIdx.x == 0) report_status(status, ATTN_ERR_BOUNDS);
+    return;
+  }
+  for (int g = 0; g < Hkv; ++g) {
+    const uint4* src = pool + (static_cast<size_t>(phys) * Hkv + g) * page_vec;
+    uint4* out = dst + ((static_cast<size_t>(b) * Hkv + g) * max_pages + p) * page_vec;
+    for (int i = static_cast<int>(threadIdx.x); i < page_vec; i += blockDim.x) out[i] = src[i];
+  }
+}
+
+}  // namespace ta
+
+using namespace ta;
+
+extern "C" {
+
+int attn_version(void) { return (0 << 16) | 1; }
+
+const char* attn_last_error(void) { return g_last_error.c_str(); }
+
+size_t attn_workspace_bytes(int B, int Hq, int Hkv, int N, int d, int mask_kind,
+                            int page_size) {
+  if (mask_kind != ATTN_MASK_PAGED_DECODE || B <= 0 || Hkv <= 0 || Hq <= 0 || N <= 0 ||
+      page_size <= 0 || d <= 0)
+    return 0;
+  return decode_layout(B, Hq, Hkv, N, d, page_size).total;
+}
+
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+             int Hkv, int N, int d, float scale, int mask_kind, int window,
+             const int32_t* cu_seqlens, const int32_t* block_table, int page_size,
+             int num_pages, void* workspace, size_t workspace_bytes, void* stream_) {
+  g_last_error.clear();
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  if (mask_kind < ATTN_MASK_NONE || mask_kind > ATTN_MASK_PAGED_DECODE)
+    return fail(ATTN_ERR_INVALID, "unknown mask_kind %d", mask_kind);
+  if (B < 0 || N < 0 || Hq <= 0 || Hkv <= 0)
+    return fail(ATTN_ERR_INVALID, "need B >= 0, N >= 0, Hq > 0, Hkv > 0");
+  if (Hq % Hkv != 0) return fail(ATTN_ERR_INVALID, "Hq (%d) %% Hkv (%d) != 0", Hq, Hkv);
+  if (d != 64 && d != 128) return fail(ATTN_ERR_UNSUPPORTED, "head dim %d (64 or 128)", d);
+  if (!std::isfinite(scale)) return fail(ATTN_ERR_INVALID, "scale is not finite");
+  if (!(scale > 0.f)) return fail(ATTN_ERR_UNSUPPORTED, "scale must be > 0");
+  if (mask_kind == ATTN_MASK_SLIDING && window < 1)
+    return fail(ATTN_ERR_INVALID, "window %d < 1", window);
+  if ((mask_kind == ATTN_MASK_DOCUMENT || mask_kind == ATTN_MASK_PAGED_DECODE) && !cu_seqlens)
+    return fail(ATTN_ERR_INVALID, "cu_seqlens is required");
+  if (B == 0 || N == 0) return ATTN_OK;  // nothing to compute
+  if (!q || !k || !v || !o || !lse) return fail(ATTN_ERR_INVALID, "null tensor pointer");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return fail(ATTN_ERR_INVALID, "tensors must be 16-byte aligned");
+  const int group = Hq / Hkv;
+  DecodeLayout L{};
+  if (mask_kind == ATTN_MASK_PAGED_DECODE) {
+    if (!block_table) return fail(ATTN_ERR_INVALID, "block_table is required");
+    if (page_size != 64) return fail(ATTN_ERR_UNSUPPORTED, "page_size %d (64)", page_size);
+    if (num_pages <= 0) return fail(ATTN_ERR_INVALID, "num_pages %d", num_pages);
+    if (group != 1 && group != 2 && group != 4 && group != 8)
+      return fail(ATTN_ERR_UNSUPPORTED, "query heads per kv head %d (1, 2, 4, 8)", group);
+    if (static_cast<long long>(num_pages) * Hkv >= (1ll << 31))
+      return fail(ATTN_ERR_UNSUPPORTED, "page pool too large");
+    L = decode_layout(B, Hq, Hkv, N, d, page_size);
+    if (L.max_splits > 65535 || Hkv > 65535 || B > 65535)
+      return fail(ATTN_ERR_UNSUPPORTED, "decode grid too large");
+    if (!workspace || workspace_bytes < L.total || !aligned16(workspace))
+      return fail(ATTN_ERR_WORKSPACE, "workspace needs %zu bytes (16-byte aligned)", L.total);
+  } else {
+    if (static_cast<long long>(B) * Hq >= (1ll << 31))
+      return fail(ATTN_ERR_UNSUPPORTED, "B*Hq too large");
+    const long long units = mask_kind == ATTN_MASK_DOCUMENT
+                                ? static_cast<long long>(Hq) * (N / kUnitRows + B)
+                                : static_cast<long long>(B) * Hq * pairs_for_rows(N);
+    if (units >= (1ll << 31) - 1) return fail(ATTN_ERR_UNSUPPORTED, "too many work units");
+  }
+  int* status = nullptr;
+  int rc = status_ptr(&status);
+  if (rc) return rc;
+
+  if (mask_kind == ATTN_MASK_PAGED_DECODE) {
+    CUtensorMap tk, tv;
+    if ((rc = encode_3d(&tk, k, d, page_size, static_cast<uint64_t>(num_pages) * Hkv, 64)))
+      return rc;
+    if ((rc = encode_3d(&tv, v, d, page_size, static_cast<uint64_t>(num_pages) * Hkv, 64)))
+      return rc;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    DecodeParams p{};
+    p.q = static_cast<const uint4*>(q);
+    p.cu = cu_seqlens;
+    p.table = block_table;
+    p.o = o;
+    p.lse = lse;
+    p.part_o = reinterpret_cast<float*>(ws + L.part_o);
+    p.part_ml = reinterpret_cast<float*>(ws + L.part_ml);
+    p.counters = reinterpret_cast<int*>(ws + L.counters);
+    p.B = B;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.max_pages = L.max_pages;
+    p.num_pages = num_pages;
+    p.max_splits = L.max_splits;
+    p.chunk_pages = kDecodeChunkPages;
+    p.scale_log2 = scale * kLog2e;
+    p.status = status;
+    p.timeout_ns = kTimeoutNs;
+    cudaError_t e = cudaMemsetAsync(p.counters, 0, sizeof(int) * static_cast<size_t>(B) * Hkv,
+                                    stream);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(counters)");
+    e = launch_decode(d, group, tk, tv, p, dim3(L.max_splits, Hkv, B), stream);
+    if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+    return ATTN_OK;
+  }
+
+  // Prefill kinds. DOCUMENT grids are an upper bound on the units (the segment lengths live
+  // on the device); surplus CTAs exit at once.
+  const int planes_q = mask_kind == ATTN_MASK_DOCUMENT ? Hq : B * Hq;
+  const int planes_kv = mask_kind == ATTN_MASK_DOCUMENT ? Hkv : B * Hkv;
+  const long long units = mask_kind == ATTN_MASK_DOCUMENT
+                              ? static_cast<long long>(Hq) * (N / kUnitRows + B)
+                              : static_cast<long long>(B) * Hq * pairs_for_rows(N);
+  CUtensorMap tq, tk, tv;
+  if ((rc = encode_3d(&tq, q, d, N, planes_q, 128))) return rc;
+  if ((rc = encode_3d(&tk, k, d, N, planes_kv, 128))) return rc;
+  if ((rc = encode_3d(&tv, v, d, N, planes_kv, 128))) return rc;
+  PrefillParams p{};
+  p.o = o;
+  p.lse = lse;
+  p.cu_seqlens = cu_seqlens;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.N = N;
+  p.group = group;
+  p.num_units = static_cast<int>(units);
+  p.window = window;
+  p.scale_log2 = scale * kLog2e;
+  p.status = status;
+  p.timeout_ns = kTimeoutNs;
+  cudaError_t e = d == 64 ? launch_prefill_d64(mask_kind, tq, tk, tv, p, p.num_units, stream)
+                          : launch_prefill_d128(mask_kind, tq, tk, tv, p, p.num_units, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
+  return ATTN_OK;
+}
+
+int attn_gather_pages(const void* pool, void* dst, const int32_t* block_table, int B,
+                      int max_pages, int Hkv, int page_size, int d, int num_pages,
+                      void* stream) {
+  g_last_error.clear();
+  if (B < 0 || max_pages < 0 || Hkv <= 0 || page_size <= 0 || d <= 0 || num_pages < 0)
+    return fail(ATTN_ERR_INVALID, "bad gather sizes");
+  if (B == 0 || max_pages == 0) return ATTN_OK;
+  if (!pool || !dst || !block_table) return fail(ATTN_ERR_INVALID, "null pointer");
+  if (!aligned16(pool) || !aligned16(dst))
+    return fail(ATTN_ERR_INVALID, "pool and dst must be 16-byte aligned");
+  if ((static_cast<long long>(page_size) * d * 2) % 16 != 0)
+    return fail(ATTN_ERR_UNSUPPORTED, "page_size * d * 2 must be a multiple of 16");
+  if (max_pages > 2147483647 || B > 65535) return fail(ATTN_ERR_UNSUPPORTED, "grid too large");
+  int* status = nullptr;
+  int rc = status_ptr(&status);
+  if (rc) return rc;
+  const int page_vec = page_size * d * 2 / 16;
+  gather_pages_kernel<<<dim3(max_pages, B), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<const uint4*>(pool), static_cast<uint4*>(dst), block_table, max_pages, Hkv,
+      page_vec, num_pages, status);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "gather launch");
+  return ATTN_OK;
+}
+
+int attn_get_status(void* stream) {
+  g_last_error.clear();
+  int* status = nullptr;
+  int rc = status_ptr(&status);
+  if (rc) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int value = 0;
+  cudaError_t e = cudaMemcpyAsync(&value, status, sizeof(int), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the status word");
+  if (value != 0) {
+    const int zero = 0;
+    e = cudaMemcpyAsync(status, &zero, sizeof(int), cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "clearing the status word");
+    fail(value, "device status %d", value);
+  }
+  return value;
+}
+
+void attn_release(void) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  for (int i = 0; i < kMaxDevices; ++i) g_status_ptr[i] = nullptr;
+}
+
+int attn_plan_kv_range(int mask_kind, int window, int r0, int bm, int row_end, int k_org,
+                       int k_end, int bn, int* lo, int* hi) {
+  if (!lo || !hi || bm <= 0 || bn <= 0 || mask_kind < 0 || mask_kind > ATTN_MASK_DOCUMENT ||
+      (mask_kind == ATTN_MASK_SLIDING && window < 1))
+    return ATTN_ERR_INVALID;
+  const KvRange r = kv_tile_range(mask_kind, window, r0, bm, row_end, k_org, k_end, bn);
+  *lo = r.lo;
+  *hi = r.hi;
+  return ATTN_OK;
+}
+
+int attn_plan_tile_kind(int mask_kind, int window, int r0, int bm, int row_end, int k_org,
+                        int k_end, int bn, int t) {
+  if (bm <= 0 || bn <= 0 || mask_kind < 0 || mask_kind > ATTN_MASK_DOCUMENT ||
+      (mask_kind == ATTN_MASK_SLIDING && window < 1))
+    return ATTN_ERR_INVALID;
+  return tile_kind(mask_kind, window, r0, bm, row_end, k_org, k_end, bn, t);
+}
+
+int attn_plan_units(int mask_kind, int B, int Hq, int N, const int32_t* cu, int32_t* out,
+                    int max_units) {
+  if (B < 0 || Hq <= 0 || N < 0 || mask_kind < 0 || mask_kind > ATTN_MASK_DOCUMENT)
+    return ATTN_ERR_INVALID;
+  std::vector<int32_t> units;
+  if (mask_kind != ATTN_MASK_DOCUMENT) {
+    const int npairs = pairs_for_rows(N);
+    for (int level = npairs - 1; level >= 0; --level)
+      for (int b = 0; b < B; ++b)
+        for (int h = 0; h < Hq; ++h) units.insert(units.end(), {b, h, level});
+  } else {
+    if (!cu) return ATTN_ERR_INVALID;
+    int tmax = 0;
+    for (int s = 0; s < B; ++s) {
+      const int len = cu[s + 1] - cu[s];
+      if (len < 0) return ATTN_ERR_SEQLENS;
+      tmax = imax(tmax, pairs_for_rows(len));
+    }
+    for (int t = tmax - 1; t >= 0; --t)
+      for (int s = 0; s < B; ++s)
+        if (pairs_for_rows(cu[s + 1] - cu[s]) > t)
+          for (int h = 0; h < Hq; ++h) units.insert(units.end(), {s, h, t});
+  }
+  const int n = static_cast<int>(units.size() / 3);
+  if (out)
+    std::memcpy(out, units.data(), sizeof(int32_t) * 3 * static_cast<size_t>(imin(n, max_units)));
+  return n;
+}
+
+}  // extern "C"

@@ -1,0 +1,480 @@
+// prefill.cuh — fused tiled attention forward for sm_103a (dense, causal, sliding window,
+// document segments).
+//
+// One CTA computes one work unit: two 128-row query tiles of one (batch or segment, query
+// head). The tiled computation with a running row max m and row sum l, rescaling the output
+// accumulator by exp(m - m_new) when the max grows, is the one described in "Flash MSA
+// Attention Kernel Implementation Tutorial" ("Understanding Flash MSA Core Mechanics"); the
+// producer / consumer split with arrive / wait barriers around a double-use shared-memory
+// ring follows "FlashAttention-3: Warp Specialization and the 75% FLOPS Barrier on Hopper"
+// ("Warp Specialization on Hopper", "The Tensor Memory Accelerator"), re-targeted to
+// Blackwell: tcgen05 MMAs with accumulators in tensor memory instead of register WGMMA.
+//
+// Roles (384 threads):
+//   warp 0      TMA producer: Q tiles once, then K_j, V_j into a STAGES-deep smem ring.
+//   warp 1      MMA issuer (one thread) and TMEM owner: S_i = Q_i K_j^T (SS MMA) and
+//               O_i += P_i V_j (P read from TMEM, V from smem).
+//   warps 4-7   softmax warpgroup for query tile 0; warps 8-11 for query tile 1. One thread
+//               owns one query row (TMEM lane): it reads its S row, applies the element mask
+//               on boundary tiles only, updates m and l with exp2, writes P (bf16) back into
+//               TMEM over S, rescales its O row only when the max grew by more than 2^8, and
+//               finally writes O / l (bf16) and the LSE.
+// TMEM columns: S_0/P_0 [0,128), S_1/P_1 [128,256), O_0 [256,256+D), O_1 [256+D,256+2D).
+//
+// Issue order per key tile j: PV_0(j-1), S_0(j), PV_1(j-1), S_1(j). tcgen05 MMAs of one
+// thread complete in order, so S_i(j) overwrites P_i(j-1) only after PV_i(j-1) has read it,
+// and "S_i(j) complete" implies "PV_i(j-1) complete": the softmax may rescale O_i right after
+// it sees S_i(j). While warpgroup 0 works on S_0(j), the tensor core runs PV_1 / S_1 and the
+// other way round.
+#pragma once
+
+#include <cuda_bf16.h>
+
+#include "ptx.cuh"
+#include "sched.h"
+
+namespace ta {
+
+struct PrefillParams {
+  void* o;                  // bf16 [planes, N, D]
+  float* lse;               // fp32 [planes, N]
+  const int* cu_seqlens;    // DOCUMENT: [B+1]
+  int B, Hq, Hkv, N, group; // N: rows per (batch, head) plane (T for DOCUMENT)
+  int num_units;            // grid size; DOCUMENT grids are an upper bound
+  int window;
+  float scale_log2;         // scale * log2(e)
+  int* status;
+  unsigned long long timeout_ns;
+};
+
+template <int D>
+struct PrefillCfg {
+  static constexpr int BM = 128;
+  static constexpr int BN = 128;
+  static constexpr int kThreads = 384;
+  static constexpr int kChunkBytes = BM * 128;        // one 64-column, 128-row swizzle panel
+  static constexpr int kPanels = D / 64;
+  static constexpr int kQBytes = BM * D * 2;
+  static constexpr int kKVBytes = BN * D * 2;
+  static constexpr int kSmemLimit = 232448;           // 227 KB opt-in maximum per block
+  static constexpr int kCtrlBytes = 1024;
+  static constexpr int kStagesFit = (kSmemLimit - 1024 - kCtrlBytes - 2 * kQBytes) / kKVBytes;
+  static constexpr int kStages = kStagesFit > 8 ? 8 : kStagesFit;
+  static constexpr int kSmemBytes = 1024 + 2 * kQBytes + kStages * kKVBytes + kCtrlBytes;
+  static constexpr int kTmemCols = 512;
+  // Launch: 384 threads x 168 registers = 64512. Warpgroup 0 (producer, MMA, two idle warps)
+  // drops to 72, the two softmax warpgroups rise to 216: 128*72 + 256*216 = 64512.
+  static constexpr uint32_t kRegsControl = 72;
+  static constexpr uint32_t kRegsSoftmax = 216;
+  static constexpr uint32_t kIdescS = idesc_bf16(BM, BN, false, false);  // Q, K both K-major
+  static constexpr uint32_t kIdescO = idesc_bf16(BM, D, false, true);    // V is MN-major
+};
+
+struct PrefillCtrl {
+  uint64_t q_full[2];
+  uint64_t kv_full[8];
+  uint64_t kv_empty[8];
+  uint64_t s_ready[2];
+  uint64_t p_ready[2];
+  uint64_t o_done[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort_flag;
+  int valid, bh, kvh, q_row0, k_org, k_end;
+};
+
+struct Unit {
+  int valid, bh, kvh, q_row0, k_org, k_end;
+};
+
+// Work unit u in launch order: pair levels from the deepest (most key tiles) down, then
+// batch / segment, then head (heads sharing a kv head are adjacent).
+template <int MASK>
+__device__ __forceinline__ Unit decode_unit(int u, const PrefillParams& p) {
+  Unit r{0, 0, 0, 0, 0, 0};
+  const int lane = static_cast<int>(lane_id());
+  if (MASK != kMaskDocument) {
+    const int per_level = p.B * p.Hq;
+    const int npairs = pairs_for_rows(p.N);
+    if (u >= per_level * npairs) return r;
+    const int level = npairs - 1 - u / per_level;
+    const int bh = u % per_level;
+    r.valid = 1;
+    r.bh = bh;
+    r.kvh = (bh / p.Hq) * p.Hkv + (bh % p.Hq) / p.group;
+    r.q_row0 = level * kUnitRows;
+    r.k_org = 0;
+    r.k_end = p.N;
+    return r;
+  }
+  // DOCUMENT: the warp scans the segments 32 at a time.
+  const int* cu = p.cu_seqlens;
+  int tmax = 0;
+  bool bad = false;
+  for (int s0 = 0; s0 < p.B; s0 += 32) {
+    const int s = s0 + lane;
+    if (s < p.B) {
+      const int len = cu[s + 1] - cu[s];
+      bad |= len < 0;
+      tmax = imax(tmax, pairs_for_rows(imax(len, 0)));
+    }
+  }
+  for (int off = 16; off; off >>= 1) tmax = imax(tmax, __shfl_xor_sync(0xffffffffu, tmax, off));
+  bad = __any_sync(0xffffffffu, bad) || cu[0] != 0 || cu[p.B] != p.N;
+  if (bad) {
+    if (u == 0 && lane == 0) report_status(p.status, -7);
+    return r;
+  }
+  int rem = u;
+  for (int t = tmax - 1; t >= 0; --t) {
+    int cnt = 0;
+    for (int s0 = 0; s0 < p.B; s0 += 32) {
+      const int s = s0 + lane;
+      const bool has = s < p.B && pairs_for_rows(cu[s + 1] - cu[s]) > t;
+      cnt += __popc(__ballot_sync(0xffffffffu, has));
+    }
+    if (rem < cnt * p.Hq) {
+      const int idx = rem / p.Hq;
+      const int h = rem % p.Hq;
+      int seen = 0, seg = -1;
+      for (int s0 = 0; s0 < p.B && seg < 0; s0 += 32) {
+        const int s = s0 + lane;
+        const bool has = s < p.B && pairs_for_rows(cu[s + 1] - cu[s]) > t;
+        unsigned m = __ballot_sync(0xffffffffu, has);
+        const int c = __popc(m);
+        if (idx < seen + c) {
+          for (int z = 0; z < idx - seen; ++z) m &= m - 1;
+          seg = s0 + __ffs(m) - 1;
+        }
+        seen += c;
+      }
+      r.valid = 1;
+      r.bh = h;
+      r.kvh = h / p.group;
+      r.k_org = cu[seg];
+      r.k_end = cu[seg + 1];
+      r.q_row0 = r.k_org + t * kUnitRows;
+      return r;
+    }
+    rem -= cnt * p.Hq;
+  }
+  return r;
+}
+
+template <int D, int MASK>
+__global__ void __launch_bounds__(384, 1)
+    prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
+                   const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
+  using C = PrefillCfg<D>;
+  constexpr int BM = C::BM, BN = C::BN, STAGES = C::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* q_s = smem;                                  // [2][kQBytes]
+  uint8_t* kv_s = smem + 2 * C::kQBytes;                // [STAGES][kKVBytes]
+  PrefillCtrl* ctl = reinterpret_cast<PrefillCtrl*>(kv_s + STAGES * C::kKVBytes);
+
+  const int warp = static_cast<int>(threadIdx.x >> 5);
+  const int lane = static_cast<int>(lane_id());
+
+  if (warp == 0) {
+    const Unit u = decode_unit<MASK>(static_cast<int>(blockIdx.x), p);
+    if (lane == 0) {
+      ctl->valid = u.valid;
+      ctl->bh = u.bh;
+      ctl->kvh = u.kvh;
+      ctl->q_row0 = u.q_row0;
+      ctl->k_org = u.k_org;
+      ctl->k_end = u.k_end;
+      ctl->abort_flag = 0;
+      for (int i = 0; i < 2; ++i) {
+        mbar_init(&ctl->q_full[i], 1);
+        mbar_init(&ctl->s_ready[i], 1);
+        mbar_init(&ctl->p_ready[i], 128);
+        mbar_init(&ctl->o_done[i], 1);
+      }
+      for (int s = 0; s < STAGES; ++s) {
+        mbar_init(&ctl->kv_full[s], 1);
+        mbar_init(&ctl->kv_empty[s], 1);
+      }
+      mbar_init(&ctl->drain, 1);
+      fence_mbar_init();
+    }
+  } else if (warp == 1) {
+    tmem_alloc(&ctl->tmem_base, C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  const uint32_t tmem = ctl->tmem_base;
+  const WaitCtl wc{p.timeout_ns, p.status, &ctl->abort_flag};
+  const WaitCtl wc_drain{p.timeout_ns, p.status, nullptr};
+
+  if (ctl->valid) {
+    const int bh = ctl->bh, kvh = ctl->kvh, q_row0 = ctl->q_row0;
+    const int k_org = ctl->k_org, k_end = ctl->k_end;
+    const int row_end = k_end;  // query rows and keys share one index space
+    KvRange rng[2];
+    int lo = 0x7fffffff, hi = -1;
+    for (int i = 0; i < 2; ++i) {
+      rng[i] = kv_tile_range(MASK, p.window, q_row0 + i * BM, BM, row_end, k_org, k_end, BN);
+      if (rng[i].hi > rng[i].lo) {
+        lo = imin(lo, rng[i].lo);
+        hi = imax(hi, rng[i].hi);
+      }
+    }
+    auto active = [&](int i, int j) { return j >= rng[i].lo && j < rng[i].hi; };
+    if (warp < 4) {
+      regs_decrease<C::kRegsControl>();
+      if (warp == 0) {
+      // ------------------------------------------------------------ TMA producer
+      if (lane == 0) {
+        prefetch_tensormap(&tm_q);
+        prefetch_tensormap(&tm_k);
+        prefetch_tensormap(&tm_v);
+        for (int i = 0; i < 2; ++i) {
+          if (rng[i].hi <= rng[i].lo) continue;
+          mbar_arrive_expect_tx(&ctl->q_full[i], C::kQBytes);
+          for (int c = 0; c < C::kPanels; ++c)
+            tma_load_3d(q_s + i * C::kQBytes + c * C::kChunkBytes, &tm_q, &ctl->q_full[i], c * 64,
+                        q_row0 + i * BM, bh);
+        }
+        int e = 0;
+        bool ok = true;
+        for (int j = lo; j < hi && ok; ++j) {
+          for (int which = 0; which < 2 && ok; ++which, ++e) {
+            const int st = e % STAGES;
+            ok = mbar_wait(&ctl->kv_empty[st], ((e / STAGES) & 1) ^ 1, wc);
+            if (!ok) break;
+            mbar_arrive_expect_tx(&ctl->kv_full[st], C::kKVBytes);
+            const CUtensorMap* m = which ? &tm_v : &tm_k;
+            for (int c = 0; c < C::kPanels; ++c)
+              tma_load_3d(kv_s + st * C::kKVBytes + c * C::kChunkBytes, m, &ctl->kv_full[st],
+                          c * 64, k_org + j * BN, kvh);
+          }
+        }
+        // Let copies still in flight land before the CTA can exit (no-op on the normal path).
+        for (int k = imax(0, e - STAGES); k < e; ++k)
+          mbar_wait(&ctl->kv_full[k % STAGES], (k / STAGES) & 1, wc_drain);
+      }
+      } else if (warp == 1) {
+      // ------------------------------------------------------------ MMA issuer
+      if (lane == 0) {
+        bool ok = true;
+        for (int i = 0; i < 2 && ok; ++i)
+          if (rng[i].hi > rng[i].lo) ok = mbar_wait(&ctl->q_full[i], 0, wc);
+        const uint32_t q_addr[2] = {smem_u32(q_s), smem_u32(q_s + C::kQBytes)};
+        int e = 0;  // ring entry of K_j
+        for (int j = lo; j <= hi && ok; ++j) {
+          const bool have_v = j > lo;
+          const bool have_k = j < hi;
+          const int ev = e - 1, ek = e;  // V_{j-1} precedes K_j in the ring
+          if (have_v) ok = mbar_wait(&ctl->kv_full[ev % STAGES], (ev / STAGES) & 1, wc);
+          if (have_k && ok) ok = mbar_wait(&ctl->kv_full[ek % STAGES], (ek / STAGES) & 1, wc);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t v_addr = smem_u32(kv_s + (ev % STAGES) * C::kKVBytes);
+          const uint32_t k_addr = smem_u32(kv_s + (ek % STAGES) * C::kKVBytes);
+          for (int i = 0; i < 2 && ok; ++i) {
+            if (have_v && active(i, j - 1)) {
+              ok = mbar_wait(&ctl->p_ready[i], (j - 1 - rng[i].lo) & 1, wc);
+              if (!ok) break;
+              tc_fence_after();
+              const uint32_t d_o = tmem + 256 + i * D;
+              const uint32_t a_p = tmem + i * 128;
+#pragma unroll
+              for (int kk = 0; kk < BN / 16; ++kk) {
+                // V panel: 128 keys x 64 columns; K step = 16 keys = 2048 bytes; the next
+                // 64-column panel (N direction) is kChunkBytes further (LBO), 8-key groups
+                // are 1024 bytes apart (SBO).
+                const uint64_t bdesc = sw128_desc(v_addr + kk * 2048, C::kChunkBytes, 1024);
+                mma_ts(d_o, a_p + kk * 8, bdesc, C::kIdescO,
+                       (j - 1 > rng[i].lo || kk > 0) ? 1u : 0u);
+              }
+              if (j == rng[i].hi) mma_commit(&ctl->o_done[i]);
+            }
+            if (have_k && active(i, j)) {
+              const uint32_t d_s = tmem + i * 128;
+#pragma unroll
+              for (int kk = 0; kk < D / 16; ++kk) {
+                // K-major panels: 16-column K step = 32 bytes inside a 128-byte swizzle row;
+                // every 4 steps move to the next 64-column panel. 8-row groups: 1024 bytes.
+                const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
+                mma_ss(d_s, sw128_desc(q_addr[i] + off, 16, 1024),
+                       sw128_desc(k_addr + off, 16, 1024), C::kIdescS, kk > 0 ? 1u : 0u);
+              }
+              mma_commit(&ctl->s_ready[i]);
+            }
+          }
+          if (!ok) break;
+          if (have_v) mma_commit(&ctl->kv_empty[ev % STAGES]);
+          if (have_k) mma_commit(&ctl->kv_empty[ek % STAGES]);
+          e += 2;
+        }
+        // Every MMA this thread issued has completed before TMEM can be released.
+        mma_commit(&ctl->drain);
+        mbar_wait(&ctl->drain, 0, wc_drain);
+      }
+      }
+    } else {
+      regs_increase<C::kRegsSoftmax>();
+      // ------------------------------------------------------------ softmax warpgroups
+      const int i = (warp - 4) >> 2;          // query tile
+      const int quarter = warp & 3;           // TMEM lanes [32*quarter, 32*quarter + 32)
+      const int r = quarter * 32 + lane;      // row inside the tile
+      const int row = q_row0 + i * BM + r;    // absolute query row
+      const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+      const uint32_t s_col = lane_base + i * 128;
+      const uint32_t o_col = lane_base + 256 + i * D;
+      const float c = p.scale_log2;
+      const KvRange my = i ? rng[1] : rng[0];
+      float m_run = -INFINITY;  // running max in log2 units (may trail the true max by < 8)
+      float l_run = 0.f;
+      bool ok = true;
+      for (int j = my.lo; j < my.hi && ok; ++j) {
+        ok = __all_sync(0xffffffffu, mbar_wait(&ctl->s_ready[i], (j - my.lo) & 1, wc));
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t s0[32], s1[32], s2[32], s3[32];
+        tmem_ld_x32(s_col + 0, s0);
+        tmem_ld_x32(s_col + 32, s1);
+        tmem_ld_x32(s_col + 64, s2);
+        tmem_ld_x32(s_col + 96, s3);
+        tmem_wait_ld_x32(s0);
+        tmem_wait_ld_x32(s1);
+        tmem_wait_ld_x32(s2);
+        tmem_wait_ld_x32(s3);
+        float* f0 = reinterpret_cast<float*>(s0);
+        float* f1 = reinterpret_cast<float*>(s1);
+        float* f2 = reinterpret_cast<float*>(s2);
+        float* f3 = reinterpret_cast<float*>(s3);
+        const int kind = tile_kind(MASK, p.window, q_row0 + i * BM, BM, row_end, k_org, k_end,
+                                   BN, j);
+        if (kind == kTileBoundary) {
+          const int key0 = k_org + j * BN;
+          const int lo_k = vis_lo(MASK, p.window, k_org, row) - key0;
+          const int hi_k = vis_hi(MASK, k_end, row) - key0;
+#pragma unroll
+          for (int t = 0; t < 32; ++t) {
+            if (t < lo_k || t > hi_k) f0[t] = -INFINITY;
+            if (t + 32 < lo_k || t + 32 > hi_k) f1[t] = -INFINITY;
+            if (t + 64 < lo_k || t + 64 > hi_k) f2[t] = -INFINITY;
+            if (t + 96 < lo_k || t + 96 > hi_k) f3[t] = -INFINITY;
+          }
+        }
+        float mx0 = f0[0], mx1 = f1[0], mx2 = f2[0], mx3 = f3[0];
+#pragma unroll
+        for (int t = 1; t < 32; ++t) {
+          mx0 = fmaxf(mx0, f0[t]);
+          mx1 = fmaxf(mx1, f1[t]);
+          mx2 = fmaxf(mx2, f2[t]);
+          mx3 = fmaxf(mx3, f3[t]);
+        }
+        const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c;
+        float alpha = 1.f;
+        // Conditional rescale: move the reference max only when the tile max exceeds it by
+        // more than 8 (a factor 256 in exp2), so most tiles skip the O read-modify-write.
+        if (m_tile > m_run + 8.f) {
+          alpha = fast_exp2(m_run - m_tile);  // 0 when m_run is -inf
+          m_run = m_tile;
+        }
+        if (j > my.lo && __any_sync(0xffffffffu, alpha < 1.f)) {
+#pragma unroll
+          for (int cc = 0; cc < D / 32; ++cc) {
+            uint32_t ov[32];
+            tmem_ld_x32(o_col + cc * 32, ov);
+            tmem_wait_ld_x32(ov);
+#pragma unroll
+            for (int t = 0; t < 32; ++t)
+              ov[t] = __float_as_uint(__uint_as_float(ov[t]) * alpha);
+            tmem_st_x32(o_col + cc * 32, ov);
+          }
+        }
+        const float msub = (m_run == -INFINITY) ? 0.f : m_run;
+        float sum0 = 0.f, sum1 = 0.f;
+        uint32_t pk[32];
+#pragma unroll
+        for (int t = 0; t < 16; ++t) {
+          const float a = fast_exp2(fmaf(f0[2 * t], c, -msub));
+          const float b = fast_exp2(fmaf(f0[2 * t + 1], c, -msub));
+          sum0 += a;
+          sum1 += b;
+          pk[t] = pack_bf16x2(a, b);
+        }
+#pragma unroll
+        for (int t = 0; t < 16; ++t) {
+          const float a = fast_exp2(fmaf(f1[2 * t], c, -msub));
+          const float b = fast_exp2(fmaf(f1[2 * t + 1], c, -msub));
+          sum0 += a;
+          sum1 += b;
+          pk[16 + t] = pack_bf16x2(a, b);
+        }
+        tmem_st_x32(s_col + 0, pk);
+#pragma unroll
+        for (int t = 0; t < 16; ++t) {
+          const float a = fast_exp2(fmaf(f2[2 * t], c, -msub));
+          const float b = fast_exp2(fmaf(f2[2 * t + 1], c, -msub));
+          sum0 += a;
+          sum1 += b;
+          pk[t] = pack_bf16x2(a, b);
+        }
+#pragma unroll
+        for (int t = 0; t < 16; ++t) {
+          const float a = fast_exp2(fmaf(f3[2 * t], c, -msub));
+          const float b = fast_exp2(fmaf(f3[2 * t + 1], c, -msub));
+          sum0 += a;
+          sum1 += b;
+          pk[16 + t] = pack_bf16x2(a, b);
+        }
+        tmem_st_x32(s_col + 32, pk);
+        l_run = l_run * alpha + (sum0 + sum1);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&ctl->p_ready[i]);
+      }
+      // ------------------------------------------------------------ epilogue
+      if (ok && my.hi > my.lo) {
+        ok = __all_sync(0xffffffffu, mbar_wait(&ctl->o_done[i], 0, wc));
+        if (ok) {
+          tc_fence_after();
+          const bool live = row < row_end;
+          const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
+          uint8_t* orow = static_cast<uint8_t*>(p.o) +
+                          (static_cast<size_t>(bh) * p.N + static_cast<size_t>(row)) * D * 2;
+#pragma unroll
+          for (int cc = 0; cc < D / 32; ++cc) {
+            uint32_t ov[32];
+            tmem_ld_x32(o_col + cc * 32, ov);
+            tmem_wait_ld_x32(ov);
+            uint32_t w[16];
+#pragma unroll
+            for (int t = 0; t < 16; ++t)
+              w[t] = pack_bf16x2(__uint_as_float(ov[2 * t]) * inv_l,
+                                 __uint_as_float(ov[2 * t + 1]) * inv_l);
+            if (live) {
+#pragma unroll
+              for (int v4 = 0; v4 < 4; ++v4)
+                st_global_v4(orow + cc * 64 + v4 * 16, w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2],
+                             w[4 * v4 + 3]);
+            }
+          }
+          if (live)
+            p.lse[static_cast<size_t>(bh) * p.N + row] =
+                l_run > 0.f ? (m_run + log2f(l_run)) * 0.69314718055994530942f : -INFINITY;
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+}  // namespace ta

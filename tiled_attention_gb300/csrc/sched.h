@@ -1,0 +1,80 @@
+// sched.h — mask-aware tile scheduling shared by the host planner and the kernels.
+//
+// Every mask kind gives each query row i a contiguous visible key interval
+// [vis_lo(i), vis_hi(i)], and both ends are nondecreasing in i. So for a tile of rows
+// [r0, r1] and keys [k0, k1]:
+//   * some pair is visible  <=>  k0 <= vis_hi(r1) and k1 >= vis_lo(r0);
+//   * every pair is visible <=>  vis_lo(r1) <= k0 and k1 <= vis_hi(r0).
+// Tiles of the first kind that are not of the second are the boundary tiles, the only ones
+// that need an element mask ("Optimizing Triton Kernels for Custom Attention Patterns on
+// H100", Pattern B: mask only the first and last key tile; Pattern A: skip the boundary check
+// inside a document). Key tiles holding no visible pair are never loaded or computed.
+#pragma once
+
+#if defined(__CUDACC__)
+#define TA_HD __host__ __device__ __forceinline__
+#else
+#define TA_HD inline
+#endif
+
+namespace ta {
+
+enum MaskKind { kMaskNone = 0, kMaskCausal = 1, kMaskSliding = 2, kMaskDocument = 3,
+                kMaskPaged = 4 };
+
+enum TileKind { kTileEmpty = 0, kTileFull = 1, kTileBoundary = 2 };
+
+TA_HD int imin(int a, int b) { return a < b ? a : b; }
+TA_HD int imax(int a, int b) { return a > b ? a : b; }
+
+// First visible key of query row i; keys are numbered in the same space as rows, and the keys
+// a tile schedule may touch start at k_org (0, or the start of the query's document segment).
+TA_HD int vis_lo(int mask, int window, int k_org, int i) {
+  return mask == kMaskSliding ? imax(k_org, i - window + 1) : k_org;
+}
+
+// Last visible key of query row i; keys end before k_end.
+TA_HD int vis_hi(int mask, int k_end, int i) {
+  return mask == kMaskNone ? k_end - 1 : imin(i, k_end - 1);
+}
+
+TA_HD bool pair_visible(int mask, int window, int k_org, int k_end, int i, int j) {
+  return j >= vis_lo(mask, window, k_org, i) && j <= vis_hi(mask, k_end, i);
+}
+
+struct KvRange {
+  int lo, hi;  // key tiles [lo, hi), numbered from k_org; empty when hi <= lo
+};
+
+// Key tiles holding at least one visible pair for the valid query rows
+// [r0, min(r0 + bm, row_end)).
+TA_HD KvRange kv_tile_range(int mask, int window, int r0, int bm, int row_end, int k_org,
+                            int k_end, int bn) {
+  KvRange r{0, 0};
+  const int r1 = imin(r0 + bm, row_end) - 1;
+  if (r1 < r0) return r;
+  const int a = vis_lo(mask, window, k_org, r0);
+  const int b = vis_hi(mask, k_end, r1);
+  if (b < a) return r;
+  r.lo = (a - k_org) / bn;
+  r.hi = (b - k_org) / bn + 1;
+  return r;
+}
+
+TA_HD int tile_kind(int mask, int window, int r0, int bm, int row_end, int k_org, int k_end,
+                    int bn, int t) {
+  const int r1 = imin(r0 + bm, row_end) - 1;
+  if (r1 < r0) return kTileEmpty;
+  const int k0 = k_org + t * bn;
+  const int k1 = k0 + bn - 1;
+  if (k0 > vis_hi(mask, k_end, r1) || k1 < vis_lo(mask, window, k_org, r0)) return kTileEmpty;
+  if (vis_lo(mask, window, k_org, r1) <= k0 && k1 <= vis_hi(mask, k_end, r0)) return kTileFull;
+  return kTileBoundary;
+}
+
+// Query rows handled by one prefill work unit: two 128-row tiles.
+constexpr int kUnitRows = 256;
+
+TA_HD int pairs_for_rows(int rows) { return (rows + kUnitRows - 1) / kUnitRows; }
+
+}  // namespace ta
