@@ -1,0 +1,407 @@
+"""Benchmark of the tiled attention forward path on GB300.
+
+One step = one pass of the whole path over one batch of synthetic input:
+  * prefill: causal attention B=2, Hq=32, Hkv=8, N=8192, d=128 (the shape the headline
+    TFLOP/s is quoted on), through attn_fwd (tile scheduler, TMA producer, tcgen05 MMA,
+    softmax, epilogue);
+  * decode: paged-KV decode, 32 sequences with contexts U[1024,16384], Hq=32, Hkv=8, d=128,
+    pages of 64 at a permuted pool, through attn_fwd (split-KV + fused combine).
+`value` is the prefill TFLOP/s (4*B*Hq*sum(visible pairs)*d / prefill time); the decode GB/s
+(valid-token K+V bytes / decode time) is reported beside it. Inputs (335 MB prefill, 1.3 GB
+decode) are larger than L2, so no flush is needed between steps.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+For N > 1 it runs under torch.distributed.run, one rank per GPU, each rank an independent
+replica of the step (the path has no exchange step); value sums all ranks' work over the
+slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "attn fwd TFLOP/s & % BF16 peak (causal N=8192 d=128); decode GB/s % HBM"
+PREFILL_NAME = "causal B2 Hq32 Hkv8 N8192 d128"
+DECODE_NAME = "paged decode B32 L U[1024,16384] Hq32 Hkv8 d128 page64 (seeded permuted pool)"
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            m = json.load(f)
+        return {"hbm_gbs": float(m["hbm_gbs"]), "bf16_tflops": float(m["bf16_tflops"]),
+                "bf16_tflops_sustained": float(m.get("bf16_tflops_sustained", m["bf16_tflops"])),
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "source": "fallback"}
+
+
+def kernel_source_hash(names):
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "tiled_attention_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, sources):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on this exact
+    kernel source; else None."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            rec = json.load(f).get(kernel)
+    except (OSError, ValueError):
+        return None
+    if not rec or rec.get("source_hash") != kernel_source_hash(sources):
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        rows = []
+        for line in (self.out or "").strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i, v in enumerate(r)
+                          if v.lower() == "active"})
+        loaded = [c for c, _, _ in rows]
+        return {"sm_mhz": float(np.median(loaded)), "sm_max_mhz": rows[0][1],
+                "reasons": reasons, "samples": len(rows)}
+
+
+def cpu_baseline_sample(w, budget_s: float, seed: int, threads: int = 0):
+    """Time the oracle on a random row sample sized for about budget_s seconds of work.
+    Returns (rows_done, flops_done, seconds)."""
+    import oracle
+    rng = np.random.default_rng(seed)
+    nrows = int(np.prod(w.lse_shape))
+
+    def row_flops(rows):
+        i = rows % w.N
+        vis = (i + 1) if w.mask_kind == 1 else np.full_like(i, w.N)
+        return 4.0 * w.d * float(vis.sum())
+
+    probe = rng.choice(nrows, size=min(nrows, 64), replace=False)
+    t0 = time.perf_counter()
+    oracle.attention(w, rows=probe, threads=threads)
+    dt = max(time.perf_counter() - t0, 1e-4)
+    n = int(min(nrows, max(64, len(probe) * budget_s / dt)))
+    rows = rng.choice(nrows, size=n, replace=False)
+    t0 = time.perf_counter()
+    oracle.attention(w, rows=rows, threads=threads)
+    dt = time.perf_counter() - t0
+    return n, row_flops(rows), dt
+
+
+def reference_arm(args, rank: int):
+    """The oracle (plain fp64 CPU) timed on the host cores: each step a bounded row sample."""
+    if rank != 0:
+        return
+    import oracle
+    from tiled_attention_gb300 import inputs as I
+    w = I.config("3c")
+    threads = oracle.max_threads()
+    per_step_s = max(0.005, 90.0 / max(1, args.steps + args.warmup))
+    rng = np.random.default_rng(77)
+    nrows = int(np.prod(w.lse_shape))
+    probe = rng.choice(nrows, size=32, replace=False)
+    t0 = time.perf_counter()
+    oracle.attention(w, rows=probe)
+    dt = max(time.perf_counter() - t0, 1e-4)
+    rows_per_step = int(max(8, 32 * per_step_s / dt))
+    flops_total = 0.0
+    t_total = 0.0
+    for step in range(args.warmup + args.steps):
+        rows = rng.choice(nrows, size=rows_per_step, replace=False)
+        t0 = time.perf_counter()
+        oracle.attention(w, rows=rows)
+        dt = time.perf_counter() - t0
+        if step >= args.warmup:
+            t_total += dt
+            i = rows % w.N
+            flops_total += 4.0 * w.d * float((i + 1).sum())
+    value = flops_total / t_total / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": t_total / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": PREFILL_NAME, "sample": f"{rows_per_step} random query rows "
+                   "per step", "l2": "n/a (CPU)"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{rows_per_step} random query rows of {PREFILL_NAME} per "
+                                   "step, fp64, materialised scores"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="own", choices=["own", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-budget", type=float, default=12.0,
+                    help="seconds of oracle work for the CPU baseline (rank 0, N=1 only)")
+    ap.add_argument("--only", choices=["prefill", "decode"], default=None,
+                    help="time one part of the step only (for profiler captures)")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        reference_arm(args, rank)
+        return
+
+    import torch
+    dist = None
+    if world > 1:
+        import torch.distributed as dist_mod
+        dist = dist_mod
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+
+    from tiled_attention_gb300 import attn, build
+    from tiled_attention_gb300 import inputs as I
+    from tiled_attention_gb300.runner import DeviceProblem
+    build.build()
+    attn.lib()
+
+    do_p = args.only in (None, "prefill")
+    do_d = args.only in (None, "decode")
+    wp = I.config("3c")
+    wd = I.config(5) if do_d else I.paged_decode_workload(5, 1, 64, 64, 32, 8, 128)
+    pp = DeviceProblem(wp, device=dev, fill_outputs=0.0)
+    pd = DeviceProblem(wd, device=dev, fill_outputs=0.0)
+    stream = torch.cuda.current_stream(dev)
+    launches_per_step = int(do_p) + int(do_d)
+
+    def step(evs=None):
+        rc = 0
+        if evs:
+            evs[0].record(stream)
+        if do_p:
+            rc |= pp.run(stream)
+        if evs:
+            evs[1].record(stream)
+        if do_d:
+            rc |= pd.run(stream)
+        if evs:
+            evs[2].record(stream)
+        return rc
+
+    for _ in range(args.warmup):
+        assert step() == 0, attn.last_error()
+    torch.cuda.synchronize(dev)
+    assert attn.attn_get_status(stream) == 0
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(dev.index) as clk:
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        for k in range(args.steps):
+            step(evs[k])
+        t_end.record(stream)
+        torch.cuda.synchronize(dev)
+    if dist:
+        dist.barrier()
+    status = attn.attn_get_status(stream)
+    assert status == 0, f"device status {status}"
+    total_ms = t_start.elapsed_time(t_end)
+    pre_ms = np.array([e[0].elapsed_time(e[1]) for e in evs])
+    dec_ms = np.array([e[1].elapsed_time(e[2]) for e in evs])
+
+    t = torch.tensor([total_ms, pre_ms.sum(), dec_ms.sum()], dtype=torch.float64, device=dev)
+    if dist:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    total_ms, pre_sum, dec_sum = (float(x) for x in t.cpu())
+
+    flops = wp.flops()
+    kv_bytes = wd.kv_bytes_valid()
+    # decode traffic that is not K/V: q, o (bf16), lse (fp32), table and lengths
+    dec_bytes = kv_bytes + wd.q.nbytes * 2 + wd.B * wd.Hq * 4 + wd.block_table.nbytes + \
+        wd.cu_seqlens.nbytes
+    pre_sum = max(pre_sum, 1e-9)
+    dec_sum = max(dec_sum, 1e-9)
+    prefill_tflops = world * args.steps * flops / (pre_sum * 1e-3) / 1e12
+    decode_gbs = world * args.steps * dec_bytes / (dec_sum * 1e-3) / 1e9
+    peaks = load_peaks()
+    pre_avg_s = pre_sum / args.steps * 1e-3
+    dec_avg_s = dec_sum / args.steps * 1e-3
+    tag = "of " + peaks["source"]
+    roofline = {
+        "bound": "tensor", "kernel": "prefill_kernel<128, causal>",
+        "achieved": flops / pre_avg_s / 1e12, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+        "frac": flops / pre_avg_s / 1e12 / peaks["bf16_tflops"],
+        "frac_of_sustained": flops / pre_avg_s / 1e12 / peaks["bf16_tflops_sustained"],
+        "peak_source": f"bf16 burst {tag}",
+        "traffic": recorded_traffic("prefill_causal_d128",
+                                    ["prefill.cuh", "ptx.cuh", "sched.h", "tmem_io.inc"]),
+        "algorithmic": f"4*B*Hq*sum(visible pairs)*d = {flops:.4e} FLOP per launch",
+    }
+    roofline_decode = {
+        "bound": "hbm", "kernel": "decode_kernel<128, 4>",
+        "achieved": dec_bytes / dec_avg_s / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+        "frac": dec_bytes / dec_avg_s / 1e9 / peaks["hbm_gbs"], "peak_source": f"HBM copy {tag}",
+        "traffic": recorded_traffic("decode_d128_g4", ["decode.cuh", "ptx.cuh"]),
+        "algorithmic": f"valid-token K+V + q/o/lse/table bytes = {dec_bytes:.4e} B per launch",
+    }
+
+    # ---- end to end: host (pinned) buffers, copies inside the timed region
+    e2e = None
+    if args.e2e_steps > 0 and args.only is None:
+        host = {}
+        for name, dp in (("p", pp), ("d", pd)):
+            for t_name in ("q", "k", "v", "o", "lse", "cu", "table"):
+                tdev = getattr(dp, t_name)
+                if tdev is not None:
+                    host[name + t_name] = torch.empty(tdev.shape, dtype=tdev.dtype,
+                                                      pin_memory=True)
+                    host[name + t_name].copy_(tdev)
+        h2d = d2h = 0
+        for name, dp in (("p", pp), ("d", pd)):
+            for t_name in ("q", "k", "v", "cu", "table"):
+                if getattr(dp, t_name) is not None:
+                    h2d += host[name + t_name].numel() * host[name + t_name].element_size()
+            for t_name in ("o", "lse"):
+                d2h += host[name + t_name].numel() * host[name + t_name].element_size()
+
+        def e2e_step(evs):
+            evs[0].record(stream)
+            for t_name in ("q", "k", "v"):
+                getattr(pp, t_name).copy_(host["p" + t_name], non_blocking=True)
+            rc = pp.run(stream)
+            host["po"].copy_(pp.o, non_blocking=True)
+            host["plse"].copy_(pp.lse, non_blocking=True)
+            evs[1].record(stream)
+            for t_name in ("q", "k", "v", "cu", "table"):
+                getattr(pd, t_name).copy_(host["d" + t_name], non_blocking=True)
+            rc |= pd.run(stream)
+            host["do"].copy_(pd.o, non_blocking=True)
+            host["dlse"].copy_(pd.lse, non_blocking=True)
+            evs[2].record(stream)
+            return rc
+
+        eevs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)]
+                for _ in range(args.e2e_steps + 2)]
+        for k in range(2):
+            assert e2e_step(eevs[k]) == 0
+        torch.cuda.synchronize(dev)
+        for k in range(args.e2e_steps):
+            assert e2e_step(eevs[2 + k]) == 0
+        torch.cuda.synchronize(dev)
+        ep = sum(e[0].elapsed_time(e[1]) for e in eevs[2:])
+        ed = sum(e[1].elapsed_time(e[2]) for e in eevs[2:])
+        te = torch.tensor([ep, ed], dtype=torch.float64, device=dev)
+        if dist:
+            dist.all_reduce(te, op=dist.ReduceOp.MAX)
+        ep, ed = (float(x) for x in te.cpu())
+        e2e = {"value": world * args.e2e_steps * flops / (ep * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "steps": args.e2e_steps,
+               "decode_gbs": world * args.e2e_steps * dec_bytes / (ed * 1e-3) / 1e9,
+               "what": "pinned host -> device copies of the step's inputs, attn_fwd, device -> "
+                       "pinned host copies of O and LSE, per part of the step"}
+
+    cpu = None
+    if rank == 0 and world == 1 and args.cpu_budget > 0:
+        import oracle
+        n, f_done, dt = cpu_baseline_sample(wp, args.cpu_budget, seed=99)
+        cpu = {"value": f_done / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.max_threads(),
+               "kind": "oracle",
+               "sample": f"{n} random query rows of {PREFILL_NAME} ({f_done:.3e} FLOP, "
+                         f"{dt:.1f} s), fp64 materialised scores"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": prefill_tflops, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": f"prefill {PREFILL_NAME} + {DECODE_NAME}",
+                       "prefill": PREFILL_NAME, "decode": DECODE_NAME,
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                       "l2": "inputs larger than L2 (335 MB prefill, 1.3 GB decode), no flush"},
+            "prefill_frac_bf16_peak": prefill_tflops / world / peaks["bf16_tflops"],
+            "decode": {"value": decode_gbs, "unit": "GB/s",
+                       "frac_hbm": decode_gbs / world / peaks["hbm_gbs"]},
+            "roofline": roofline,
+            "roofline_decode": roofline_decode,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clk.summary(),
+        }
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
