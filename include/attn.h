@@ -109,6 +109,28 @@ int attn_gather_pages(const void *pool, void *dst, const int32_t *block_table, i
                       int max_pages, int Hkv, int page_size, int d, int num_pages,
                       void *stream);
 
+/*
+ * attn_paged_decode_noalloc — paged decode for callers that cannot allocate device memory.
+ * (No counterpart on the pages: this is a packaging of attn_fwd's PAGED_DECODE case.)
+ *
+ * Same arguments, layouts and results as attn_fwd with mask_kind = ATTN_MASK_PAGED_DECODE,
+ * without the workspace: the split-KV scratch is a fixed 16 MiB (16777216-byte) array inside
+ * the library, held by every GPU that loads it until the process exits. Meant for callers that get no scratch buffer from
+ * their host framework (a custom-op interface, another framework's memory pool) or must not
+ * let cudaMalloc / cudaFree synchronise the device on a serving path. It allocates nothing.
+ *  - Returns ATTN_ERR_UNSUPPORTED, with a message, when attn_workspace_bytes() of the request
+ *    exceeds the array; nothing is launched then.
+ *  - The first call on each device looks up the array's device address (cudaGetSymbolAddress)
+ *    with that device current; make that first call before any stream capture.
+ *  - Every call shares the one array per device and it keeps the last call's contents (the
+ *    call zeroes what must start at zero on its stream). Calls whose kernels overlap on the
+ *    GPU (different streams, or host threads without ordering) race on it: order them.
+ */
+int attn_paged_decode_noalloc(const void *q, const void *k, const void *v, void *o, float *lse,
+                              int B, int Hq, int Hkv, int N, int d, float scale,
+                              const int32_t *cu_seqlens, const int32_t *block_table,
+                              int page_size, int num_pages, void *stream);
+
 /* Synchronises `stream`, then returns and clears the device status word (ATTN_OK or one of
  * ATTN_ERR_TIMEOUT / ATTN_ERR_BOUNDS / ATTN_ERR_SEQLENS), or ATTN_ERR_CUDA if the stream
  * reported a CUDA error. */

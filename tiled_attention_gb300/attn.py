@@ -46,6 +46,8 @@ _SIGS = {
                                 ctypes.POINTER(_i)]),
     "attn_plan_tile_kind": (_i, [_i, _i, _i, _i, _i, _i, _i, _i, _i]),
     "attn_plan_units": (_i, [_i, _i, _i, _i, _p, _p, _i]),
+    "attn_paged_decode_noalloc": (_i, [_p, _p, _p, _p, _p, _i, _i, _i, _i, _i, ctypes.c_float,
+                                       _p, _p, _i, _i, _p]),
 }
 
 
@@ -109,6 +111,15 @@ def attn_fwd(q, k, v, o, lse, B, Hq, Hkv, N, d, scale, mask_kind, window=0, cu_s
                           ctypes.c_float(scale), mask_kind, window, _ptr(cu_seqlens),
                           _ptr(block_table), page_size, num_pages, _ptr(workspace), ws_bytes,
                           _stream(stream))
+
+
+def attn_paged_decode_noalloc(q, k, v, o, lse, B, Hq, Hkv, N, d, scale, cu_seqlens, block_table,
+                              page_size, num_pages, stream=None) -> int:
+    """Paged decode without a workspace argument (the library's fixed scratch is used)."""
+    return lib().attn_paged_decode_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq,
+                                           Hkv, N, d, ctypes.c_float(scale), _ptr(cu_seqlens),
+                                           _ptr(block_table), page_size, num_pages,
+                                           _stream(stream))
 
 
 def attn_workspace_bytes(B, Hq, Hkv, N, d, mask_kind, page_size=0) -> int:

@@ -386,3 +386,60 @@ int attn_plan_units(int mask_kind, int B, int Hq, int N, const int32_t* cu, int3
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------ allocation-free decode
+// Some callers cannot hand this library a workspace and cannot let it call cudaMalloc: code
+// running inside another framework's device-memory pool or a custom-op interface that passes
+// no scratch buffer, and serving loops where the implicit device synchronisation of
+// cudaMalloc / cudaFree is not acceptable. attn_paged_decode_noalloc serves them: its
+// split-KV partials and tickets live in the fixed array below, which every GPU that loads
+// this library holds until the process exits.
+namespace ta {
+namespace {
+constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;  // 16 MiB
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+void* g_noalloc_scratch_ptr[kMaxDevices];
+
+// Device address of the scratch array on the current device. In host code the array's name
+// is only a host-side stand-in, so the address comes from cudaGetSymbolAddress, once per
+// device, with that device current.
+int noalloc_scratch(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(ATTN_ERR_UNSUPPORTED, "device %d", dev);
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_noalloc_scratch_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(decode scratch)");
+    g_noalloc_scratch_ptr[dev] = p;
+  }
+  *out = g_noalloc_scratch_ptr[dev];
+  return ATTN_OK;
+}
+}  // namespace
+}  // namespace ta
+
+extern "C" int attn_paged_decode_noalloc(const void* q, const void* k, const void* v, void* o,
+                                         float* lse, int B, int Hq, int Hkv, int N, int d,
+                                         float scale, const int32_t* cu_seqlens,
+                                         const int32_t* block_table, int page_size,
+                                         int num_pages, void* stream) {
+  g_last_error.clear();
+  const size_t need =
+      attn_workspace_bytes(B, Hq, Hkv, N, d, ATTN_MASK_PAGED_DECODE, page_size);
+  if (need > kNoAllocScratchBytes)
+    return fail(ATTN_ERR_UNSUPPORTED,
+                "this decode needs %zu bytes of split-KV scratch; the allocation-free entry "
+                "point has %zu (fewer sequences, kv heads or a shorter longest context fit)",
+                need, kNoAllocScratchBytes);
+  void* scratch = nullptr;
+  int rc = noalloc_scratch(&scratch);
+  if (rc) return rc;
+  // The decode path zeroes the tickets it needs (cudaMemsetAsync, no allocation) on `stream`
+  // before its kernel; the partials are written before they are read.
+  return attn_fwd(q, k, v, o, lse, B, Hq, Hkv, N, d, scale, ATTN_MASK_PAGED_DECODE, 0,
+                  cu_seqlens, block_table, page_size, num_pages, scratch, kNoAllocScratchBytes,
+                  stream);
+}
