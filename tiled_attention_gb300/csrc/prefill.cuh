@@ -161,6 +161,28 @@ __device__ __forceinline__ Unit decode_unit(int u, const PrefillParams& p) {
   return r;
 }
 
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// 32 scores -> 16 packed bf16x2 probabilities exp2(c*s - m); partial sums in sa / sb.
+__device__ __forceinline__ void exp2_pack_32(const float* f, float2 cc, float2 mm, float2& sa,
+                                             float2& sb, uint32_t* pk) {
+#pragma unroll
+  for (int t = 0; t < 16; t += 2) {
+    const float2 x0 = __ffma2_rn(make_float2(f[2 * t], f[2 * t + 1]), cc, mm);
+    const float2 x1 = __ffma2_rn(make_float2(f[2 * t + 2], f[2 * t + 3]), cc, mm);
+    const float2 p0 = make_float2(fast_exp2(x0.x), fast_exp2(x0.y));
+    const float2 p1 = make_float2(fast_exp2(x1.x), fast_exp2(x1.y));
+    sa = __fadd2_rn(sa, p0);
+    sb = __fadd2_rn(sb, p1);
+    pk[t] = pack_bf16x2(p0.x, p0.y);
+    pk[t + 1] = pack_bf16x2(p1.x, p1.y);
+  }
+}
+
 template <int D, int MASK>
 __global__ void __launch_bounds__(384, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -295,6 +317,8 @@ __global__ void __launch_bounds__(384, 1)
                        (j - 1 > rng[i].lo || kk > 0) ? 1u : 0u);
               }
               if (j == rng[i].hi) mma_commit(&ctl->o_done[i]);
+              // Release V_{j-1} as soon as its last reader is issued.
+              if (i == 1 || !active(1, j - 1)) mma_commit(&ctl->kv_empty[ev % STAGES]);
             }
             if (have_k && active(i, j)) {
               const uint32_t d_s = tmem + i * 128;
@@ -310,7 +334,6 @@ __global__ void __launch_bounds__(384, 1)
             }
           }
           if (!ok) break;
-          if (have_v) mma_commit(&ctl->kv_empty[ev % STAGES]);
           if (have_k) mma_commit(&ctl->kv_empty[ek % STAGES]);
           e += 2;
         }
@@ -365,15 +388,19 @@ __global__ void __launch_bounds__(384, 1)
             if (t + 96 < lo_k || t + 96 > hi_k) f3[t] = -INFINITY;
           }
         }
-        float mx0 = f0[0], mx1 = f1[0], mx2 = f2[0], mx3 = f3[0];
+        // Row max: four independent chains of 3-input max over the 128 scores.
+        float mx0 = fmax3(f0[0], f0[1], f0[2]), mx1 = fmax3(f1[0], f1[1], f1[2]);
+        float mx2 = fmax3(f2[0], f2[1], f2[2]), mx3 = fmax3(f3[0], f3[1], f3[2]);
 #pragma unroll
-        for (int t = 1; t < 32; ++t) {
-          mx0 = fmaxf(mx0, f0[t]);
-          mx1 = fmaxf(mx1, f1[t]);
-          mx2 = fmaxf(mx2, f2[t]);
-          mx3 = fmaxf(mx3, f3[t]);
+        for (int t = 3; t < 31; t += 2) {
+          mx0 = fmax3(mx0, f0[t], f0[t + 1]);
+          mx1 = fmax3(mx1, f1[t], f1[t + 1]);
+          mx2 = fmax3(mx2, f2[t], f2[t + 1]);
+          mx3 = fmax3(mx3, f3[t], f3[t + 1]);
         }
-        const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c;
+        mx0 = fmax3(mx0, f0[31], f1[31]);
+        mx2 = fmax3(mx2, f2[31], f3[31]);
+        const float m_tile = fmax3(fmaxf(mx0, mx1), mx2, mx3) * c;
         float alpha = 1.f;
         // Conditional rescale: move the reference max only when the tile max exceeds it by
         // more than 8 (a factor 256 in exp2), so most tiles skip the O read-modify-write.
@@ -394,43 +421,19 @@ __global__ void __launch_bounds__(384, 1)
           }
         }
         const float msub = (m_run == -INFINITY) ? 0.f : m_run;
-        float sum0 = 0.f, sum1 = 0.f;
+        // p = exp2(c*s - m) two at a time: one packed FMA, two MUFU ex2, one packed add into
+        // two independent partial sums, one bf16x2 pack.
+        const float2 cc = make_float2(c, c);
+        const float2 mm = make_float2(-msub, -msub);
+        float2 sa = make_float2(0.f, 0.f), sb = make_float2(0.f, 0.f);
         uint32_t pk[32];
-#pragma unroll
-        for (int t = 0; t < 16; ++t) {
-          const float a = fast_exp2(fmaf(f0[2 * t], c, -msub));
-          const float b = fast_exp2(fmaf(f0[2 * t + 1], c, -msub));
-          sum0 += a;
-          sum1 += b;
-          pk[t] = pack_bf16x2(a, b);
-        }
-#pragma unroll
-        for (int t = 0; t < 16; ++t) {
-          const float a = fast_exp2(fmaf(f1[2 * t], c, -msub));
-          const float b = fast_exp2(fmaf(f1[2 * t + 1], c, -msub));
-          sum0 += a;
-          sum1 += b;
-          pk[16 + t] = pack_bf16x2(a, b);
-        }
+        exp2_pack_32(f0, cc, mm, sa, sb, pk);
+        exp2_pack_32(f1, cc, mm, sa, sb, pk + 16);
         tmem_st_x32(s_col + 0, pk);
-#pragma unroll
-        for (int t = 0; t < 16; ++t) {
-          const float a = fast_exp2(fmaf(f2[2 * t], c, -msub));
-          const float b = fast_exp2(fmaf(f2[2 * t + 1], c, -msub));
-          sum0 += a;
-          sum1 += b;
-          pk[t] = pack_bf16x2(a, b);
-        }
-#pragma unroll
-        for (int t = 0; t < 16; ++t) {
-          const float a = fast_exp2(fmaf(f3[2 * t], c, -msub));
-          const float b = fast_exp2(fmaf(f3[2 * t + 1], c, -msub));
-          sum0 += a;
-          sum1 += b;
-          pk[16 + t] = pack_bf16x2(a, b);
-        }
+        exp2_pack_32(f2, cc, mm, sa, sb, pk);
+        exp2_pack_32(f3, cc, mm, sa, sb, pk + 16);
         tmem_st_x32(s_col + 32, pk);
-        l_run = l_run * alpha + (sum0 + sum1);
+        l_run = l_run * alpha + ((sa.x + sa.y) + (sb.x + sb.y));
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(&ctl->p_ready[i]);
