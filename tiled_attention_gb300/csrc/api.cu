@@ -201,8 +201,8 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
     if (!block_table) return fail(ATTN_ERR_INVALID, "block_table is required");
     if (page_size != 64) return fail(ATTN_ERR_UNSUPPORTED, "page_size %d (64)", page_size);
     if (num_pages <= 0) return fail(ATTN_ERR_INVALID, "num_pages %d", num_pages);
-    if (group != 1 && group != 2 && group != 4 && group != 8)
-      return fail(ATTN_ERR_UNSUPPORTED, "query heads per kv head %d (1, 2, 4, 8)", group);
+    if (group != 1 && group != 2 && group != 4 && group != 8 && group != 16)
+      return fail(ATTN_ERR_UNSUPPORTED, "query heads per kv head %d (1, 2, 4, 8, 16)", group);
     if (static_cast<long long>(num_pages) * Hkv >= (1ll << 31))
       return fail(ATTN_ERR_UNSUPPORTED, "page pool too large");
     L = decode_layout(B, Hq, Hkv, N, d, page_size);

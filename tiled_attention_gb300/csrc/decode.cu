@@ -24,6 +24,7 @@ cudaError_t launch_d(int group, const CUtensorMap& k, const CUtensorMap& v,
     case 2: return launch_one<D, 2>(k, v, p, grid, stream);
     case 4: return launch_one<D, 4>(k, v, p, grid, stream);
     case 8: return launch_one<D, 8>(k, v, p, grid, stream);
+    case 16: return launch_one<D, 16>(k, v, p, grid, stream);
     default: return cudaErrorInvalidValue;
   }
 }

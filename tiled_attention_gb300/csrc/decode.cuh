@@ -8,11 +8,15 @@
 // a shared-memory ring, so every K/V byte crosses HBM once.
 //
 // Grid (split, kv head g, sequence b): a CTA handles `chunk_pages` pages of one (b, g) for
-// all G = Hq/Hkv query heads of the group. Decode reads each K/V byte once and does ~4 FLOP
-// per byte, so it is HBM-bound and runs on the CUDA cores (mixed bf16 x bf16 + fp32 FMA), not
-// the tensor cores. Per page: scores for (token, head) pairs, a per-head running max and sum
-// (the online softmax of "Flash MSA Attention Kernel Implementation Tutorial", "Understanding
-// Flash MSA Core Mechanics", in exp2 form), then P.V into per-thread fp32 accumulators.
+// all G = Hq/Hkv query heads of the group. Decode reads each K/V byte once and is HBM-bound;
+// the arithmetic only has to stay off the critical path. It runs as warp-level bf16 MMAs
+// (mma.sync m16n8k16, fp32 accumulate) with the G heads as the rows of a 16-row tile: an
+// instruction-count choice, not a throughput one (scalar FMAs needed ~600 instructions per
+// thread per page and made the consumers, not HBM, the bottleneck). Each of the four consumer
+// warps owns a 16-token slice of every page and keeps its own running max, sum and O (the
+// online softmax of "Flash MSA Attention Kernel Implementation Tutorial", "Understanding Flash
+// MSA Core Mechanics", in exp2 form), so pages need no cross-warp synchronisation; the four
+// partial results are merged once per chunk with the same rescaling identity.
 //
 // Combine: each split writes its unnormalised O, max m and sum l (log2 units) to the
 // workspace; the last split to finish (atomic ticket per (b, g)) merges them in split order:
@@ -45,22 +49,23 @@ struct DecodeParams {
 template <int D, int G>
 struct DecodeCfg {
   static constexpr int kPage = 64;
-  static constexpr int kConsumers = 256;
+  static constexpr int kWarps = 4;  // consumer warp w owns tokens [16w, 16w + 16) of each page
+  static constexpr int kConsumers = kWarps * 32;
   static constexpr int kThreads = kConsumers + 32;
   static constexpr int kPanels = D / 64;
   static constexpr int kPanelBytes = kPage * 128;           // 64 tokens x 64 columns
   static constexpr int kPageBytes = kPage * D * 2;          // one (page, kv-head) of K or V
   static constexpr int kStageBytes = 2 * kPageBytes;        // K and V
   static constexpr int kStages = (96 * 1024) / kStageBytes; // 3 (D=128), 6 (D=64)
-  static constexpr int kGP = G < 2 ? 2 : G;                 // heads per p row, padded to pairs
-  static constexpr int kPairs = kPage * G;
-  static constexpr int kPairsPerThread = (kPairs + kConsumers - 1) / kConsumers;
-  static constexpr int kDPairs = D / 2;
-  static constexpr int kTokenGroups = kConsumers / kDPairs;
+  static constexpr int kKSteps = D / 16;                    // k-steps of S = Q K^T
+  static constexpr int kNTiles = D / 8;                     // n-tiles of O += P V
+  static constexpr bool kHi = G > 8;                        // rows 8..15 of the tile are heads
   static constexpr int kRingBytes = kStages * kStageBytes;
-  static constexpr int kQPitch = D * 2 + 16;  // padded so the G query rows hit distinct banks
-  static constexpr int kMiscBytes = 2048 + G * kQPitch;
-  static constexpr int kSmemBytes = 1024 + kRingBytes + kMiscBytes;  // ring + ctrl/p/red/q
+  // misc area: control 256 | per-warp row max [4][16] | per-warp row sum [4][16]
+  static constexpr int kOffMax = 256, kOffSum = 512, kMiscBytes = 768;
+  static constexpr int kSmemBytes = 1024 + kRingBytes + kMiscBytes;
+  static_assert(G >= 1 && G <= 16, "query heads per kv head");
+  static_assert(2 * G * D * 4 <= kRingBytes, "merge buffer reuses the ring");
 };
 
 struct DecodeCtrl {
@@ -70,31 +75,41 @@ struct DecodeCtrl {
   int is_last;
 };
 
-// c + a.lo * b.lo + a.hi * b.hi (bf16 pairs, exact products, fp32 accumulation).
-__device__ __forceinline__ float dot2_bf16(uint32_t a, uint32_t b, float c) {
-  asm("{\n .reg .b16 al, ah, bl, bh;\n mov.b32 {al, ah}, %1;\n mov.b32 {bl, bh}, %2;\n"
-      " fma.rn.f32.bf16 %0, al, bl, %0;\n fma.rn.f32.bf16 %0, ah, bh, %0;\n}"
-      : "+f"(c)
-      : "r"(a), "r"(b));
-  return c;
+// D(16x8, fp32) += A(16x16, bf16, row-major) * B(16x8, bf16, column-major).
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4],
+                                               uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
+      "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// (c00, c01, c10, c11) += (p.lo * v.lo, p.lo * v.hi, p.hi * v.lo, p.hi * v.hi).
-__device__ __forceinline__ void outer2_bf16(uint32_t p, uint32_t v, float& c00, float& c01,
-                                            float& c10, float& c11) {
-  asm("{\n .reg .b16 pl, ph, vl, vh;\n mov.b32 {pl, ph}, %4;\n mov.b32 {vl, vh}, %5;\n"
-      " fma.rn.f32.bf16 %0, pl, vl, %0;\n fma.rn.f32.bf16 %1, pl, vh, %1;\n"
-      " fma.rn.f32.bf16 %2, ph, vl, %2;\n fma.rn.f32.bf16 %3, ph, vh, %3;\n}"
-      : "+f"(c00), "+f"(c01), "+f"(c10), "+f"(c11)
-      : "r"(p), "r"(v));
+__device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], uint32_t saddr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(saddr));
+}
+
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t (&r)[4], uint32_t saddr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(saddr));
 }
 
 __device__ __forceinline__ uint16_t bf16_bits(float x) {
   return static_cast<uint16_t>(pack_bf16x2(x, 0.f) & 0xFFFFu);
 }
 
+// Byte offset of the 16-byte chunk holding columns [d0, d0 + 8) of `token` in a page that TMA
+// wrote with 128-byte swizzle (64-column panels of 64 rows x 128 bytes).
+__device__ __forceinline__ uint32_t page_chunk(int token, int d0) {
+  return static_cast<uint32_t>((d0 >> 6) * (64 * 128) + token * 128 +
+                               ((((d0 & 63) >> 3) ^ (token & 7)) << 4));
+}
+
 template <int D, int G>
-__global__ void __launch_bounds__(288, 2)
+__global__ void __launch_bounds__(160, 2)
     decode_kernel(const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const DecodeParams p) {
   using C = DecodeCfg<D, G>;
@@ -132,15 +147,13 @@ __global__ void __launch_bounds__(288, 2)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* misc = ring + C::kRingBytes;
   DecodeCtrl* ctl = reinterpret_cast<DecodeCtrl*>(misc);
-  uint16_t* p_buf = reinterpret_cast<uint16_t*>(misc + 256);              // [64][kGP]
-  float* red_max = reinterpret_cast<float*>(misc + 256 + 64 * 8 * 2);     // [G][8]
-  float* red_l = red_max + 8 * 8;                                         // [G][8]
-  uint8_t* q_s = misc + 2048;                                             // [G][kQPitch]
+  float* red_m = reinterpret_cast<float*>(misc + C::kOffMax);  // [4 warps][16 rows]
+  float* red_l = reinterpret_cast<float*>(misc + C::kOffSum);  // [4 warps][16 rows]
 
   if (tid == C::kConsumers) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&ctl->full[s], 1);
-      mbar_init(&ctl->empty[s], 8);
+      mbar_init(&ctl->empty[s], C::kWarps);
     }
     ctl->abort_flag = 0;
     ctl->is_last = 0;
@@ -150,7 +163,7 @@ __global__ void __launch_bounds__(288, 2)
   const WaitCtl wc{p.timeout_ns, p.status, &ctl->abort_flag};
   const WaitCtl wc_drain{p.timeout_ns, p.status, nullptr};
 
-  if (warp == 8) {
+  if (warp == C::kWarps) {
     // ---------------------------------------------------------------- TMA producer
     if (lane == 0) {
       prefetch_tensormap(&tm_k);
@@ -186,165 +199,213 @@ __global__ void __launch_bounds__(288, 2)
   }
 
   // ------------------------------------------------------------------ consumers
-  const int h_qk = tid % G;  // head of this thread's score pairs (256 % G == 0)
-  const bool qk_live = tid < C::kPairs;
-  for (int idx = tid; idx < G * (D / 8); idx += C::kConsumers) {
-    const int hh = idx / (D / 8), ch = idx % (D / 8);
-    *reinterpret_cast<uint4*>(q_s + hh * C::kQPitch + ch * 16) =
-        p.q[(static_cast<size_t>(b) * p.Hq + g * G + hh) * (D / 8) + ch];
-  }
-  named_barrier_sync(1, C::kConsumers);
-  const uint8_t* q_row = q_s + h_qk * C::kQPitch;
-  const int dp = tid % C::kDPairs;
-  const int tg = tid / C::kDPairs;
-  const int v_off = (dp / 32) * C::kPanelBytes + (dp % 4) * 4;  // panel + bytes inside chunk
-  const int v_chunk = (dp % 32) / 4;
-  float acc[G][2];
-  float m_run[G];
+  const int r = lane >> 2;  // tile rows r and r + 8 (heads), fragment columns 2q, 2q + 1
+  const int q = lane & 3;
+  const size_t head0 = static_cast<size_t>(b) * p.Hq + static_cast<size_t>(g) * G;
+  // Q as the A operand: rows = heads (zero past G), k = head dimension.
+  uint32_t qa[C::kKSteps][4];
+  {
+    const uint32_t* q32 = reinterpret_cast<const uint32_t*>(p.q);
 #pragma unroll
-  for (int hh = 0; hh < G; ++hh) {
-    acc[hh][0] = acc[hh][1] = 0.f;
-    m_run[hh] = -INFINITY;
+    for (int kk = 0; kk < C::kKSteps; ++kk) {
+      const bool lo = r < G, hi = C::kHi && r + 8 < G;
+      qa[kk][0] = lo ? q32[(head0 + r) * (D / 2) + kk * 8 + q] : 0u;
+      qa[kk][2] = lo ? q32[(head0 + r) * (D / 2) + kk * 8 + 4 + q] : 0u;
+      qa[kk][1] = hi ? q32[(head0 + r + 8) * (D / 2) + kk * 8 + q] : 0u;
+      qa[kk][3] = hi ? q32[(head0 + r + 8) * (D / 2) + kk * 8 + 4 + q] : 0u;
+    }
   }
-  float l_part = 0.f;
+  float o[C::kNTiles][4];
+#pragma unroll
+  for (int nt = 0; nt < C::kNTiles; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
+  float m_lo = -INFINITY, m_hi = -INFINITY;  // running max (log2 units), trails by < 8
+  float l_lo = 0.f, l_hi = 0.f;              // this thread's share of the running sums
   const float c = p.scale_log2;
+  const uint32_t ring_u32 = smem_u32(ring);
+  const int tok_w = warp * 16;
+  // ldmatrix row addresses: lane -> (matrix, row); see the fragment maps below.
+  const int mrow = lane & 7, msel = lane >> 3;
+  const int k_token = tok_w + 8 * (msel >> 1) + mrow;  // K: matrices (n-tile, k half)
+  const int k_half = (msel & 1) * 8;
+  const int v_token = tok_w + 8 * (msel & 1) + mrow;   // V: matrices (n-tile, token half)
+  const int v_sub = (msel >> 1) * 8;
   bool ok = true;
 
   for (int k = 0; k < n; ++k) {
     const int st = k % S;
     ok = __all_sync(0xffffffffu, mbar_wait(&ctl->full[st], (k / S) & 1, wc));
-    // Every consumer warp must take the same number of named barriers: a warp that gave up
-    // still walks the page loop, without touching the ring.
-    const uint8_t* kp = ring + st * C::kStageBytes;
-    const uint8_t* vp = kp + C::kPageBytes;
-    const int tok0 = (pg0 + k) * C::kPage;
-
-    float sc[C::kPairsPerThread];
-    float mloc = -INFINITY;
-#pragma unroll
-    for (int u = 0; u < C::kPairsPerThread; ++u) {
-      const int idx = tid + u * C::kConsumers;
-      const int t = idx / G;
-      float s = -INFINITY;
-      if (idx < C::kPairs && ok && tok0 + t < L) {
-        float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-#pragma unroll
-        for (int pn = 0; pn < C::kPanels; ++pn) {
-#pragma unroll
-          for (int ch = 0; ch < 8; ++ch) {
-            const uint4 kv = *reinterpret_cast<const uint4*>(
-                kp + pn * C::kPanelBytes + t * 128 + ((ch ^ (t & 7)) << 4));
-            const uint4 qv = *reinterpret_cast<const uint4*>(q_row + pn * 128 + ch * 16);
-            a0 = dot2_bf16(qv.x, kv.x, a0);
-            a1 = dot2_bf16(qv.y, kv.y, a1);
-            a2 = dot2_bf16(qv.z, kv.z, a2);
-            a3 = dot2_bf16(qv.w, kv.w, a3);
-          }
-        }
-        s = ((a0 + a1) + (a2 + a3)) * c;
-      }
-      sc[u] = s;
-      mloc = fmaxf(mloc, s);
-    }
-#pragma unroll
-    for (int off = G; off < 32; off <<= 1)
-      mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, off));
-    if (lane < G) red_max[lane * 8 + warp] = mloc;
-    named_barrier_sync(1, C::kConsumers);
-
-    float alpha[G];
-#pragma unroll
-    for (int hh = 0; hh < G; ++hh) {
-      const float4 x = *reinterpret_cast<const float4*>(red_max + hh * 8);
-      const float4 y = *reinterpret_cast<const float4*>(red_max + hh * 8 + 4);
-      const float pm = fmaxf(fmaxf(fmaxf(x.x, x.y), fmaxf(x.z, x.w)),
-                             fmaxf(fmaxf(y.x, y.y), fmaxf(y.z, y.w)));
-      const float mn = fmaxf(m_run[hh], pm);
-      alpha[hh] = (mn == -INFINITY) ? 1.f : fast_exp2(m_run[hh] - mn);
-      m_run[hh] = mn;
-    }
-    {
-      float m_own = m_run[0], a_own = alpha[0];
-#pragma unroll
-      for (int hh = 1; hh < G; ++hh) {
-        m_own = (hh == h_qk) ? m_run[hh] : m_own;
-        a_own = (hh == h_qk) ? alpha[hh] : a_own;
-      }
-      const float msub = (m_own == -INFINITY) ? 0.f : m_own;
-      l_part *= a_own;
-#pragma unroll
-      for (int u = 0; u < C::kPairsPerThread; ++u) {
-        const int idx = tid + u * C::kConsumers;
-        if (idx < C::kPairs) {
-          const float pv = fast_exp2(sc[u] - msub);
-          l_part += pv;
-          p_buf[(idx / G) * C::kGP + h_qk] = bf16_bits(pv);
-        }
-      }
-      if (G == 1 && qk_live) p_buf[(tid / G) * C::kGP + 1] = 0;
-    }
-    named_barrier_sync(1, C::kConsumers);
-
-#pragma unroll
-    for (int hh = 0; hh < G; ++hh) {
-      acc[hh][0] *= alpha[hh];
-      acc[hh][1] *= alpha[hh];
-    }
     if (ok) {
-#pragma unroll 4
-      for (int t = tg; t < C::kPage; t += C::kTokenGroups) {
-        const uint32_t vw =
-            *reinterpret_cast<const uint32_t*>(vp + v_off + t * 128 + ((v_chunk ^ (t & 7)) << 4));
-        const uint32_t* prow = reinterpret_cast<const uint32_t*>(p_buf + t * C::kGP);
+      const uint32_t kp = ring_u32 + st * C::kStageBytes;
+      const uint32_t vp = kp + C::kPageBytes;
+      // S = Q K^T for this warp's 16 tokens: two 8-token n-tiles.
+      float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int w = 0; w < C::kGP / 2; ++w) {
-          float dummy0 = 0.f, dummy1 = 0.f;
-          float& c10 = (2 * w + 1 < G) ? acc[(2 * w + 1) % G][0] : dummy0;
-          float& c11 = (2 * w + 1 < G) ? acc[(2 * w + 1) % G][1] : dummy1;
-          outer2_bf16(prow[w], vw, acc[2 * w][0], acc[2 * w][1], c10, c11);
+      for (int kk = 0; kk < C::kKSteps; ++kk) {
+        uint32_t kb[4];
+        ldmatrix_x4(kb, kp + page_chunk(k_token, kk * 16 + k_half));
+        mma_bf16_16816(s0, qa[kk], kb[0], kb[1]);
+        mma_bf16_16816(s1, qa[kk], kb[2], kb[3]);
+      }
+      // Scale, mask keys past the context, update the running max of rows r (and r + 8).
+      const int tok = (pg0 + k) * C::kPage + tok_w + 2 * q;
+      float x[2][4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int te = tok + (e & 1);
+        x[0][e] = (te < L) ? s0[e] * c : -INFINITY;
+        x[1][e] = (te + 8 < L) ? s1[e] * c : -INFINITY;
+      }
+      float mx_lo = fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[1][0], x[1][1]));
+      float mx_hi = fmaxf(fmaxf(x[0][2], x[0][3]), fmaxf(x[1][2], x[1][3]));
+      mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 1));
+      mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 2));
+      mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 1));
+      mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 2));
+      float a_lo = 1.f, a_hi = 1.f;
+      // Conditional rescale: move the reference max only when it grows by more than 8.
+      if (mx_lo > m_lo + 8.f) {
+        a_lo = fast_exp2(m_lo - mx_lo);
+        m_lo = mx_lo;
+      }
+      if (C::kHi && mx_hi > m_hi + 8.f) {
+        a_hi = fast_exp2(m_hi - mx_hi);
+        m_hi = mx_hi;
+      }
+      if (__any_sync(0xffffffffu, a_lo < 1.f || a_hi < 1.f)) {
+#pragma unroll
+        for (int nt = 0; nt < C::kNTiles; ++nt) {
+          o[nt][0] *= a_lo;
+          o[nt][1] *= a_lo;
+          o[nt][2] *= a_hi;
+          o[nt][3] *= a_hi;
         }
+        l_lo *= a_lo;
+        l_hi *= a_hi;
+      }
+      const float sub_lo = (m_lo == -INFINITY) ? 0.f : m_lo;
+      const float sub_hi = (m_hi == -INFINITY) ? 0.f : m_hi;
+      const bool live_lo = r < G, live_hi = C::kHi && r + 8 < G;
+      float pr[2][4];
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        pr[nt][0] = live_lo ? fast_exp2(x[nt][0] - sub_lo) : 0.f;
+        pr[nt][1] = live_lo ? fast_exp2(x[nt][1] - sub_lo) : 0.f;
+        pr[nt][2] = live_hi ? fast_exp2(x[nt][2] - sub_hi) : 0.f;
+        pr[nt][3] = live_hi ? fast_exp2(x[nt][3] - sub_hi) : 0.f;
+      }
+      l_lo += (pr[0][0] + pr[0][1]) + (pr[1][0] + pr[1][1]);
+      l_hi += (pr[0][2] + pr[0][3]) + (pr[1][2] + pr[1][3]);
+      // The S accumulators of the two n-tiles are, as bf16 pairs, the A fragment of P.
+      const uint32_t pa[4] = {pack_bf16x2(pr[0][0], pr[0][1]), pack_bf16x2(pr[0][2], pr[0][3]),
+                              pack_bf16x2(pr[1][0], pr[1][1]), pack_bf16x2(pr[1][2], pr[1][3])};
+      // O += P V over this warp's 16 tokens, two 8-column n-tiles per ldmatrix.
+#pragma unroll
+      for (int pair = 0; pair < C::kNTiles / 2; ++pair) {
+        uint32_t vb[4];
+        ldmatrix_x4_trans(vb, vp + page_chunk(v_token, pair * 16 + v_sub));
+        mma_bf16_16816(o[2 * pair], pa, vb[0], vb[1]);
+        mma_bf16_16816(o[2 * pair + 1], pa, vb[2], vb[3]);
       }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&ctl->empty[st]);
   }
 
-  // ------------------------------------------------------------------ split result
-  float* red_acc = reinterpret_cast<float*>(ring);  // [kTokenGroups][G][D]; ring is idle now
-#pragma unroll
-  for (int off = G; off < 32; off <<= 1) l_part += __shfl_xor_sync(0xffffffffu, l_part, off);
+  // ------------------------------------------------------------------ merge the four warps
+  l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 1);
+  l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 2);
+  l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 1);
+  l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 2);
   named_barrier_sync(1, C::kConsumers);  // every consumer is past its last ring read
-  if (lane < G) red_l[lane * 8 + warp] = l_part;
-#pragma unroll
-  for (int hh = 0; hh < G; ++hh)
-    *reinterpret_cast<float2*>(red_acc + (tg * G + hh) * D + 2 * dp) =
-        make_float2(acc[hh][0], acc[hh][1]);
+  if (q == 0) {
+    red_m[warp * 16 + r] = m_lo;
+    red_l[warp * 16 + r] = l_lo;
+    red_m[warp * 16 + r + 8] = m_hi;
+    red_l[warp * 16 + r + 8] = l_hi;
+  }
   named_barrier_sync(1, C::kConsumers);
+  float M_lo = red_m[r], M_hi = red_m[r + 8];
+#pragma unroll
+  for (int w = 1; w < C::kWarps; ++w) {
+    M_lo = fmaxf(M_lo, red_m[w * 16 + r]);
+    M_hi = fmaxf(M_hi, red_m[w * 16 + r + 8]);
+  }
+  {
+    const float f_lo = (m_lo == -INFINITY) ? 0.f : fast_exp2(m_lo - M_lo);
+    const float f_hi = (m_hi == -INFINITY) ? 0.f : fast_exp2(m_hi - M_hi);
+#pragma unroll
+    for (int nt = 0; nt < C::kNTiles; ++nt) {
+      o[nt][0] *= f_lo;
+      o[nt][1] *= f_lo;
+      o[nt][2] *= f_hi;
+      o[nt][3] *= f_hi;
+    }
+  }
+  // Sum the warps' rescaled O in a fixed order (3 + 2 -> 1 + 0, then 1 -> 0), through the idle
+  // ring: [2 slots][16 rows][D] fp32.
+  float* buf = reinterpret_cast<float*>(ring);
+#pragma unroll
+  for (int half = C::kWarps / 2; half >= 1; half >>= 1) {
+    if (warp >= half && warp < 2 * half) {
+      float* dst = buf + (warp - half) * 16 * D;
+#pragma unroll
+      for (int nt = 0; nt < C::kNTiles; ++nt) {
+        *reinterpret_cast<float2*>(dst + r * D + nt * 8 + 2 * q) = make_float2(o[nt][0], o[nt][1]);
+        *reinterpret_cast<float2*>(dst + (r + 8) * D + nt * 8 + 2 * q) =
+            make_float2(o[nt][2], o[nt][3]);
+      }
+    }
+    named_barrier_sync(1, C::kConsumers);
+    if (warp < half) {
+      const float* src = buf + warp * 16 * D;
+#pragma unroll
+      for (int nt = 0; nt < C::kNTiles; ++nt) {
+        const float2 lo = *reinterpret_cast<const float2*>(src + r * D + nt * 8 + 2 * q);
+        const float2 hi = *reinterpret_cast<const float2*>(src + (r + 8) * D + nt * 8 + 2 * q);
+        o[nt][0] += lo.x;
+        o[nt][1] += lo.y;
+        o[nt][2] += hi.x;
+        o[nt][3] += hi.y;
+      }
+    }
+    named_barrier_sync(1, C::kConsumers);
+  }
 
   const size_t bg = static_cast<size_t>(b) * p.Hkv + g;
   const bool single = nsplit == 1;
-  for (int idx = tid; idx < G * D; idx += C::kConsumers) {
-    const int hh = idx / D, d = idx % D;
-    float ou = 0.f;
+  if (warp == 0) {
+    float L_lo = 0.f, L_hi = 0.f;
 #pragma unroll
-    for (int q = 0; q < C::kTokenGroups; ++q) ou += red_acc[(q * G + hh) * D + d];
-    float l = 0.f;
+    for (int w = 0; w < C::kWarps; ++w) {
+      const float mw_lo = red_m[w * 16 + r], mw_hi = red_m[w * 16 + r + 8];
+      if (mw_lo != -INFINITY) L_lo += red_l[w * 16 + r] * fast_exp2(mw_lo - M_lo);
+      if (mw_hi != -INFINITY) L_hi += red_l[w * 16 + r + 8] * fast_exp2(mw_hi - M_hi);
+    }
 #pragma unroll
-    for (int w = 0; w < 8; ++w) l += red_l[hh * 8 + w];
-    float mrun = m_run[0];
+    for (int half = 0; half < 2; ++half) {
+      const int row = r + 8 * half;
+      if (row >= G) continue;
+      const float Lr = half ? L_hi : L_lo;
+      const float Mr = half ? M_hi : M_lo;
+      const size_t orow = head0 + row;
+      if (single) {
+        const float inv = Lr > 0.f ? 1.f / Lr : 0.f;
+        uint32_t* o32 = reinterpret_cast<uint32_t*>(o16 + orow * D);
 #pragma unroll
-    for (int h2 = 1; h2 < G; ++h2) mrun = (h2 == hh) ? m_run[h2] : mrun;
-    if (single) {
-      o16[(static_cast<size_t>(b) * p.Hq + g * G + hh) * D + d] = bf16_bits(ou / l);
-      if (d == 0)
-        p.lse[static_cast<size_t>(b) * p.Hq + g * G + hh] =
-            (mrun + log2f(l)) * 0.69314718055994530942f;
-    } else {
-      const size_t base = (bg * p.max_splits + split) * G + hh;
-      p.part_o[base * D + d] = ou;
-      if (d == 0) {
-        p.part_ml[2 * base] = mrun;
-        p.part_ml[2 * base + 1] = l;
+        for (int nt = 0; nt < C::kNTiles; ++nt)
+          o32[nt * 4 + q] = pack_bf16x2(o[nt][2 * half] * inv, o[nt][2 * half + 1] * inv);
+        if (q == 0)
+          p.lse[orow] = Lr > 0.f ? (Mr + log2f(Lr)) * 0.69314718055994530942f : -INFINITY;
+      } else {
+        const size_t base = (bg * p.max_splits + split) * G + row;
+#pragma unroll
+        for (int nt = 0; nt < C::kNTiles; ++nt)
+          *reinterpret_cast<float2*>(p.part_o + base * D + nt * 8 + 2 * q) =
+              make_float2(o[nt][2 * half], o[nt][2 * half + 1]);
+        if (q == 0) {
+          p.part_ml[2 * base] = Mr;
+          p.part_ml[2 * base + 1] = Lr;
+        }
       }
     }
   }
@@ -359,6 +420,7 @@ __global__ void __launch_bounds__(288, 2)
   named_barrier_sync(1, C::kConsumers);
   if (!ctl->is_last) return;
   __threadfence();
+  // Last split of (b, g): merge the splits in split order.
   for (int idx = tid; idx < G * D; idx += C::kConsumers) {
     const int hh = idx / D, d = idx % D;
     const size_t base0 = (bg * p.max_splits) * G + hh;
@@ -371,10 +433,8 @@ __global__ void __launch_bounds__(288, 2)
       Ls += __ldcg(p.part_ml + 2 * bs + 1) * w;
       Os += __ldcg(p.part_o + bs * D + d) * w;
     }
-    o16[(static_cast<size_t>(b) * p.Hq + g * G + hh) * D + d] = bf16_bits(Os / Ls);
-    if (d == 0)
-      p.lse[static_cast<size_t>(b) * p.Hq + g * G + hh] =
-          (M + log2f(Ls)) * 0.69314718055994530942f;
+    o16[(head0 + hh) * D + d] = bf16_bits(Os / Ls);
+    if (d == 0) p.lse[head0 + hh] = (M + log2f(Ls)) * 0.69314718055994530942f;
   }
   if (tid == 0) p.counters[bg] = 0;
 }
