@@ -122,6 +122,21 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
+def max_over_ranks(values, dist=None, device="cpu"):
+    """Element-wise max of per-rank timings (the slowest rank sets the job time)."""
+    import torch
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    if dist is not None and dist.is_initialized() and dist.get_world_size() > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.cpu()]
+
+
+def replica_throughput(world: int, steps: int, units_per_step: float, seconds: float) -> float:
+    """Whole-job throughput of `world` independent replicas: every rank processed
+    units_per_step per step; the job took the slowest rank's time."""
+    return world * steps * units_per_step / seconds
+
+
 def cpu_baseline_sample(w, budget_s: float, seed: int, threads: int = 0):
     """Time the oracle on a random row sample sized for about budget_s seconds of work.
     Returns (rows_done, flops_done, seconds)."""
@@ -277,10 +292,7 @@ def main():
     pre_ms = np.array([e[0].elapsed_time(e[1]) for e in evs])
     dec_ms = np.array([e[1].elapsed_time(e[2]) for e in evs])
 
-    t = torch.tensor([total_ms, pre_ms.sum(), dec_ms.sum()], dtype=torch.float64, device=dev)
-    if dist:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    total_ms, pre_sum, dec_sum = (float(x) for x in t.cpu())
+    total_ms, pre_sum, dec_sum = max_over_ranks([total_ms, pre_ms.sum(), dec_ms.sum()], dist, dev)
 
     flops = wp.flops()
     kv_bytes = wd.kv_bytes_valid()
@@ -289,8 +301,8 @@ def main():
         wd.cu_seqlens.nbytes
     pre_sum = max(pre_sum, 1e-9)
     dec_sum = max(dec_sum, 1e-9)
-    prefill_tflops = world * args.steps * flops / (pre_sum * 1e-3) / 1e12
-    decode_gbs = world * args.steps * dec_bytes / (dec_sum * 1e-3) / 1e9
+    prefill_tflops = replica_throughput(world, args.steps, flops, pre_sum * 1e-3) / 1e12
+    decode_gbs = replica_throughput(world, args.steps, dec_bytes, dec_sum * 1e-3) / 1e9
     peaks = load_peaks()
     pre_avg_s = pre_sum / args.steps * 1e-3
     dec_avg_s = dec_sum / args.steps * 1e-3
@@ -358,14 +370,12 @@ def main():
         torch.cuda.synchronize(dev)
         ep = sum(e[0].elapsed_time(e[1]) for e in eevs[2:])
         ed = sum(e[1].elapsed_time(e[2]) for e in eevs[2:])
-        te = torch.tensor([ep, ed], dtype=torch.float64, device=dev)
-        if dist:
-            dist.all_reduce(te, op=dist.ReduceOp.MAX)
-        ep, ed = (float(x) for x in te.cpu())
-        e2e = {"value": world * args.e2e_steps * flops / (ep * 1e-3) / 1e12, "unit": "TFLOP/s",
+        ep, ed = max_over_ranks([ep, ed], dist, dev)
+        e2e = {"value": replica_throughput(world, args.e2e_steps, flops, ep * 1e-3) / 1e12,
+               "unit": "TFLOP/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "steps": args.e2e_steps,
-               "decode_gbs": world * args.e2e_steps * dec_bytes / (ed * 1e-3) / 1e9,
+               "decode_gbs": replica_throughput(world, args.e2e_steps, dec_bytes, ed * 1e-3) / 1e9,
                "what": "pinned host -> device copies of the step's inputs, attn_fwd, device -> "
                        "pinned host copies of O and LSE, per part of the step"}
 

@@ -140,6 +140,12 @@ int attn_get_status(void *stream);
  * valid until the next call on that thread. */
 const char *attn_last_error(void);
 
+/* Failure-detection self-test: launches one thread that waits, through the same bounded
+ * wait every kernel uses, on a barrier nothing arrives on. After timeout_ns (1 ns .. 10 s) it
+ * gives up and the status word reads ATTN_ERR_TIMEOUT; the GPU context stays usable.
+ * Asynchronous; read the outcome with attn_get_status(stream). */
+int attn_selftest_wait_timeout(unsigned long long timeout_ns, void *stream);
+
 /* Frees the library's cached device state (status word) on the current device. */
 void attn_release(void);
 

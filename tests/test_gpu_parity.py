@@ -234,6 +234,17 @@ def test_bad_cu_seqlens_reports_status():
     assert attn.attn_get_status() == attn.ATTN_ERR_SEQLENS
 
 
+def test_bounded_wait_times_out_and_context_survives():
+    """A wait on a barrier nothing arrives on gives up after its limit, records
+    ATTN_ERR_TIMEOUT, and the context keeps working (a normal call right after passes)."""
+    assert attn.attn_selftest_wait_timeout(20_000_000) == 0  # 20 ms
+    torch.cuda.synchronize()
+    assert attn.attn_get_status() == attn.ATTN_ERR_TIMEOUT
+    assert attn.attn_get_status() == 0
+    w = I.config(1)
+    compare(w, run(w))
+
+
 def test_side_stream():
     w = I.config(1)
     s = torch.cuda.Stream()

@@ -46,6 +46,7 @@ _SIGS = {
                                 ctypes.POINTER(_i)]),
     "attn_plan_tile_kind": (_i, [_i, _i, _i, _i, _i, _i, _i, _i, _i]),
     "attn_plan_units": (_i, [_i, _i, _i, _i, _p, _p, _i]),
+    "attn_selftest_wait_timeout": (_i, [ctypes.c_ulonglong, _p]),
     "attn_paged_decode_noalloc": (_i, [_p, _p, _p, _p, _p, _i, _i, _i, _i, _i, ctypes.c_float,
                                        _p, _p, _i, _i, _p]),
 }
@@ -130,6 +131,10 @@ def attn_gather_pages(pool, dst, block_table, B, max_pages, Hkv, page_size, d, n
                       stream=None) -> int:
     return lib().attn_gather_pages(_ptr(pool), _ptr(dst), _ptr(block_table), B, max_pages, Hkv,
                                    page_size, d, num_pages, _stream(stream))
+
+
+def attn_selftest_wait_timeout(timeout_ns: int, stream=None) -> int:
+    return lib().attn_selftest_wait_timeout(timeout_ns, _stream(stream))
 
 
 def attn_get_status(stream=None) -> int:

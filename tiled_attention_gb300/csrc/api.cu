@@ -155,11 +155,43 @@ __global__ void gather_pages_kernel(const uint4* __restrict__ pool, uint4* __res
   }
 }
 
+// Self-test of the bounded pipeline wait: one thread waits on an mbarrier that nothing
+// arrives on, with the same mbar_wait the kernels use, and must give up after timeout_ns,
+// record ATTN_ERR_TIMEOUT and return.
+__global__ void wait_timeout_selftest_kernel(unsigned long long timeout_ns, int* status) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const WaitCtl wc{timeout_ns, status, &abort_flag};
+    mbar_wait(&bar, 0, wc);
+  }
+}
+
 }  // namespace ta
 
 using namespace ta;
 
 extern "C" {
+
+int attn_selftest_wait_timeout(unsigned long long timeout_ns, void* stream) {
+  g_last_error.clear();
+  if (timeout_ns == 0 || timeout_ns > 10000000000ull)
+    return fail(ATTN_ERR_INVALID, "timeout_ns must be in (0, 1e10]");
+  int* status = nullptr;
+  int rc = status_ptr(&status);
+  if (rc) return rc;
+  wait_timeout_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(timeout_ns,
+                                                                               status);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "self-test launch");
+  return ATTN_OK;
+}
 
 int attn_version(void) { return (0 << 16) | 1; }
 
