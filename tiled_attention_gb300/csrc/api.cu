@@ -295,8 +295,9 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
   const long long units = mask_kind == ATTN_MASK_DOCUMENT
                               ? static_cast<long long>(Hq) * (N / kUnitRows + B)
                               : static_cast<long long>(B) * Hq * pairs_for_rows(N);
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk, tv, to;
   if ((rc = encode_3d(&tq, q, d, N, planes_q, 128))) return rc;
+  if ((rc = encode_3d(&to, o, d, N, planes_q, 32))) return rc;
   if ((rc = encode_3d(&tk, k, d, N, planes_kv, 128))) return rc;
   if ((rc = encode_3d(&tv, v, d, N, planes_kv, 128))) return rc;
   PrefillParams p{};
@@ -313,8 +314,8 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
   p.scale_log2 = scale * kLog2e;
   p.status = status;
   p.timeout_ns = kTimeoutNs;
-  cudaError_t e = d == 64 ? launch_prefill_d64(mask_kind, tq, tk, tv, p, p.num_units, stream)
-                          : launch_prefill_d128(mask_kind, tq, tk, tv, p, p.num_units, stream);
+  cudaError_t e = d == 64 ? launch_prefill_d64(mask_kind, tq, tk, tv, to, p, p.num_units, stream)
+                          : launch_prefill_d128(mask_kind, tq, tk, tv, to, p, p.num_units, stream);
   if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
   return ATTN_OK;
 }

@@ -9,13 +9,14 @@
 
 namespace ta {
 
-// Launch prefill_kernel<d, mask> with `grid` CTAs; returns the launch error.
+// Launch prefill_kernel<d, mask> with `grid` CTAs; returns the launch error. `o` maps the
+// output with 32-row boxes (one softmax warp's rows).
 cudaError_t launch_prefill_d64(int mask, const CUtensorMap& q, const CUtensorMap& k,
-                               const CUtensorMap& v, const PrefillParams& p, int grid,
-                               cudaStream_t stream);
+                               const CUtensorMap& v, const CUtensorMap& o,
+                               const PrefillParams& p, int grid, cudaStream_t stream);
 cudaError_t launch_prefill_d128(int mask, const CUtensorMap& q, const CUtensorMap& k,
-                                const CUtensorMap& v, const PrefillParams& p, int grid,
-                                cudaStream_t stream);
+                                const CUtensorMap& v, const CUtensorMap& o,
+                                const PrefillParams& p, int grid, cudaStream_t stream);
 
 // Launch decode_kernel<d, group> on grid (max_splits, Hkv, B).
 cudaError_t launch_decode(int d, int group, const CUtensorMap& k, const CUtensorMap& v,

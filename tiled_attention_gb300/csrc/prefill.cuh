@@ -187,7 +187,8 @@ template <int D, int MASK>
 __global__ void __launch_bounds__(384, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
                    const __grid_constant__ CUtensorMap tm_k,
-                   const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
+                   const __grid_constant__ CUtensorMap tm_v,
+                   const __grid_constant__ CUtensorMap tm_o, const PrefillParams p) {
   using C = PrefillCfg<D>;
   constexpr int BM = C::BM, BN = C::BN, STAGES = C::kStages;
   extern __shared__ uint8_t smem_raw[];
@@ -200,6 +201,9 @@ __global__ void __launch_bounds__(384, 1)
   const int warp = static_cast<int>(threadIdx.x >> 5);
   const int lane = static_cast<int>(lane_id());
 
+  // Loads issued before the block-wide barrier: the unit's Q tiles and the first STAGES ring
+  // entries (all slots start empty), so they are in flight while TMEM is allocated.
+  int e_early = 0;
   if (warp == 0) {
     const Unit u = decode_unit<MASK>(static_cast<int>(blockIdx.x), p);
     if (lane == 0) {
@@ -222,6 +226,30 @@ __global__ void __launch_bounds__(384, 1)
       }
       mbar_init(&ctl->drain, 1);
       fence_mbar_init();
+      if (u.valid) {
+        prefetch_tensormap(&tm_q);
+        prefetch_tensormap(&tm_k);
+        prefetch_tensormap(&tm_v);
+        int lo = 0x7fffffff, hi = -1;
+        for (int i = 0; i < 2; ++i) {
+          const KvRange rg = kv_tile_range(MASK, p.window, u.q_row0 + i * BM, BM, u.k_end,
+                                           u.k_org, u.k_end, BN);
+          if (rg.hi <= rg.lo) continue;
+          lo = imin(lo, rg.lo);
+          hi = imax(hi, rg.hi);
+          mbar_arrive_expect_tx(&ctl->q_full[i], C::kQBytes);
+          for (int c = 0; c < C::kPanels; ++c)
+            tma_load_3d(q_s + i * C::kQBytes + c * C::kChunkBytes, &tm_q, &ctl->q_full[i], c * 64,
+                        u.q_row0 + i * BM, u.bh);
+        }
+        for (; e_early < STAGES && e_early < 2 * (hi - lo); ++e_early) {
+          mbar_arrive_expect_tx(&ctl->kv_full[e_early], C::kKVBytes);
+          const CUtensorMap* m = (e_early & 1) ? &tm_v : &tm_k;
+          for (int c = 0; c < C::kPanels; ++c)
+            tma_load_3d(kv_s + e_early * C::kKVBytes + c * C::kChunkBytes, m,
+                        &ctl->kv_full[e_early], c * 64, u.k_org + (lo + e_early / 2) * BN, u.kvh);
+        }
+      }
     }
   } else if (warp == 1) {
     tmem_alloc(&ctl->tmem_base, C::kTmemCols);
@@ -254,29 +282,18 @@ __global__ void __launch_bounds__(384, 1)
       if (warp == 0) {
       // ------------------------------------------------------------ TMA producer
       if (lane == 0) {
-        prefetch_tensormap(&tm_q);
-        prefetch_tensormap(&tm_k);
-        prefetch_tensormap(&tm_v);
-        for (int i = 0; i < 2; ++i) {
-          if (rng[i].hi <= rng[i].lo) continue;
-          mbar_arrive_expect_tx(&ctl->q_full[i], C::kQBytes);
-          for (int c = 0; c < C::kPanels; ++c)
-            tma_load_3d(q_s + i * C::kQBytes + c * C::kChunkBytes, &tm_q, &ctl->q_full[i], c * 64,
-                        q_row0 + i * BM, bh);
-        }
-        int e = 0;
+        // Ring entry e holds K_{lo + e/2} (e even) or V_{lo + e/2} (e odd).
+        int e = e_early;
         bool ok = true;
-        for (int j = lo; j < hi && ok; ++j) {
-          for (int which = 0; which < 2 && ok; ++which, ++e) {
-            const int st = e % STAGES;
-            ok = mbar_wait(&ctl->kv_empty[st], ((e / STAGES) & 1) ^ 1, wc);
-            if (!ok) break;
-            mbar_arrive_expect_tx(&ctl->kv_full[st], C::kKVBytes);
-            const CUtensorMap* m = which ? &tm_v : &tm_k;
-            for (int c = 0; c < C::kPanels; ++c)
-              tma_load_3d(kv_s + st * C::kKVBytes + c * C::kChunkBytes, m, &ctl->kv_full[st],
-                          c * 64, k_org + j * BN, kvh);
-          }
+        for (; e < 2 * (hi - lo) && ok; ++e) {
+          const int st = e % STAGES;
+          ok = mbar_wait(&ctl->kv_empty[st], ((e / STAGES) & 1) ^ 1, wc);
+          if (!ok) break;
+          mbar_arrive_expect_tx(&ctl->kv_full[st], C::kKVBytes);
+          const CUtensorMap* m = (e & 1) ? &tm_v : &tm_k;
+          for (int c = 0; c < C::kPanels; ++c)
+            tma_load_3d(kv_s + st * C::kKVBytes + c * C::kChunkBytes, m, &ctl->kv_full[st],
+                        c * 64, k_org + (lo + e / 2) * BN, kvh);
         }
         // Let copies still in flight land before the CTA can exit (no-op on the normal path).
         for (int k = imax(0, e - STAGES); k < e; ++k)
@@ -445,6 +462,14 @@ __global__ void __launch_bounds__(384, 1)
           tc_fence_after();
           const bool live = row < row_end;
           const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
+          // The warp's 32 rows go out through shared memory and one TMA store per 64-column
+          // panel, written into Q_i's buffer (dead: its last S MMA completed before o_done) in
+          // the 128-byte-swizzled layout the store expects. Rows past the tensor's extent are
+          // clipped by the store; a DOCUMENT warp whose rows run past its segment writes
+          // them one thread per row instead, so the next segment's rows stay untouched.
+          const int warp_row0 = q_row0 + i * BM + quarter * 32;
+          const bool staged = MASK != kMaskDocument || warp_row0 + 31 < row_end;
+          uint8_t* stage = q_s + i * C::kQBytes;
           uint8_t* orow = static_cast<uint8_t*>(p.o) +
                           (static_cast<size_t>(bh) * p.N + static_cast<size_t>(row)) * D * 2;
 #pragma unroll
@@ -457,11 +482,30 @@ __global__ void __launch_bounds__(384, 1)
             for (int t = 0; t < 16; ++t)
               w[t] = pack_bf16x2(__uint_as_float(ov[2 * t]) * inv_l,
                                  __uint_as_float(ov[2 * t + 1]) * inv_l);
-            if (live) {
+            if (staged) {
+              // 16-byte chunk k of row r sits at chunk k ^ (r % 8) of the row's 128 bytes.
+              const uint32_t rbase = smem_u32(stage + (cc >> 1) * C::kChunkBytes + r * 128);
+#pragma unroll
+              for (int v4 = 0; v4 < 4; ++v4)
+                st_shared_v4(rbase + ((((cc & 1) * 4 + v4) ^ (r & 7)) << 4), w[4 * v4],
+                             w[4 * v4 + 1], w[4 * v4 + 2], w[4 * v4 + 3]);
+            } else if (live) {
 #pragma unroll
               for (int v4 = 0; v4 < 4; ++v4)
                 st_global_v4(orow + cc * 64 + v4 * 16, w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2],
                              w[4 * v4 + 3]);
+            }
+          }
+          if (staged && warp_row0 < row_end) {
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              for (int c = 0; c < C::kPanels; ++c)
+                tma_store_3d(&tm_o, stage + c * C::kChunkBytes + quarter * 32 * 128, c * 64,
+                             warp_row0, bh);
+              bulk_commit_group();
+              // The buffer must stay valid until the stores have read it.
+              bulk_wait_group_read0();
             }
           }
           if (live)

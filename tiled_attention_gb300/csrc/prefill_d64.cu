@@ -6,25 +6,26 @@ namespace ta {
 namespace {
 template <int MASK>
 cudaError_t launch_one(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                       const PrefillParams& p, int grid, cudaStream_t stream) {
+                       const CUtensorMap& o, const PrefillParams& p, int grid,
+                       cudaStream_t stream) {
   static unsigned long long done = 0;
   auto kern = prefill_kernel<64, MASK>;
   constexpr int smem = PrefillCfg<64>::kSmemBytes;
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), smem, &done);
   if (e != cudaSuccess) return e;
-  kern<<<grid, PrefillCfg<64>::kThreads, smem, stream>>>(q, k, v, p);
+  kern<<<grid, PrefillCfg<64>::kThreads, smem, stream>>>(q, k, v, o, p);
   return cudaGetLastError();
 }
 }  // namespace
 
 cudaError_t launch_prefill_d64(int mask, const CUtensorMap& q, const CUtensorMap& k,
-                               const CUtensorMap& v, const PrefillParams& p, int grid,
-                               cudaStream_t stream) {
+                               const CUtensorMap& v, const CUtensorMap& o,
+                               const PrefillParams& p, int grid, cudaStream_t stream) {
   switch (mask) {
-    case kMaskNone: return launch_one<kMaskNone>(q, k, v, p, grid, stream);
-    case kMaskCausal: return launch_one<kMaskCausal>(q, k, v, p, grid, stream);
-    case kMaskSliding: return launch_one<kMaskSliding>(q, k, v, p, grid, stream);
-    case kMaskDocument: return launch_one<kMaskDocument>(q, k, v, p, grid, stream);
+    case kMaskNone: return launch_one<kMaskNone>(q, k, v, o, p, grid, stream);
+    case kMaskCausal: return launch_one<kMaskCausal>(q, k, v, o, p, grid, stream);
+    case kMaskSliding: return launch_one<kMaskSliding>(q, k, v, o, p, grid, stream);
+    case kMaskDocument: return launch_one<kMaskDocument>(q, k, v, o, p, grid, stream);
     default: return cudaErrorInvalidValue;
   }
 }
