@@ -12,7 +12,7 @@
 //
 // Roles (384 threads):
 //   warp 0      TMA producer: Q tiles once, then K_j, V_j into a STAGES-deep smem ring.
-//   warp 1      MMA issuer (one thread) and TMEM owner: S_i = Q_i K_j^T (SS MMA) and
+//   warp 1      MMA issuer (one elected lane) and TMEM owner: S_i = Q_i K_j^T (SS MMA) and
 //               O_i += P_i V_j (P read from TMEM, V from smem).
 //   warps 4-7   softmax warpgroup for query tile 0; warps 8-11 for query tile 1. One thread
 //               owns one query row (TMEM lane): it reads its S row, applies the element mask
@@ -63,9 +63,9 @@ struct PrefillCfg {
   static constexpr int kSmemBytes = 1024 + 2 * kQBytes + kStages * kKVBytes + kCtrlBytes;
   static constexpr int kTmemCols = 512;
   // Launch: 384 threads x 168 registers = 64512. Warpgroup 0 (producer, MMA, two idle warps)
-  // drops to 72, the two softmax warpgroups rise to 216: 128*72 + 256*216 = 64512.
-  static constexpr uint32_t kRegsControl = 72;
-  static constexpr uint32_t kRegsSoftmax = 216;
+  // drops to 88, the two softmax warpgroups rise to 208: 128*88 + 256*208 = 64512.
+  static constexpr uint32_t kRegsControl = 88;
+  static constexpr uint32_t kRegsSoftmax = 208;
   static constexpr uint32_t kIdescS = idesc_bf16(BM, BN, false, false);  // Q, K both K-major
   static constexpr uint32_t kIdescO = idesc_bf16(BM, D, false, true);    // V is MN-major
 };
@@ -301,63 +301,72 @@ __global__ void __launch_bounds__(384, 1)
       }
       } else if (warp == 1) {
       // ------------------------------------------------------------ MMA issuer
-      if (lane == 0) {
-        bool ok = true;
-        for (int i = 0; i < 2 && ok; ++i)
-          if (rng[i].hi > rng[i].lo) ok = mbar_wait(&ctl->q_full[i], 0, wc);
-        const uint32_t q_addr[2] = {smem_u32(q_s), smem_u32(q_s + C::kQBytes)};
-        int e = 0;  // ring entry of K_j
-        for (int j = lo; j <= hi && ok; ++j) {
-          const bool have_v = j > lo;
-          const bool have_k = j < hi;
-          const int ev = e - 1, ek = e;  // V_{j-1} precedes K_j in the ring
-          if (have_v) ok = mbar_wait(&ctl->kv_full[ev % STAGES], (ev / STAGES) & 1, wc);
-          if (have_k && ok) ok = mbar_wait(&ctl->kv_full[ek % STAGES], (ek / STAGES) & 1, wc);
+      // The whole warp runs this loop, so descriptors and loop state are warp-uniform; one
+      // elected lane issues each tcgen05 instruction (see mma_ss). Waits are agreed on by the
+      // whole warp so it never diverges.
+      constexpr unsigned kFull = 0xffffffffu;
+      bool ok = true;
+      if (rng[0].hi > rng[0].lo) ok = __all_sync(kFull, mbar_wait(&ctl->q_full[0], 0, wc));
+      if (ok && rng[1].hi > rng[1].lo) ok = __all_sync(kFull, mbar_wait(&ctl->q_full[1], 0, wc));
+      // Descriptors of the two Q tiles; a K step adds its byte offset / 16 to the start field,
+      // which stays inside its 14 bits for any shared-memory address.
+      const uint64_t q_desc0 = sw128_desc(smem_u32(q_s), 16, 1024);
+      const uint64_t q_desc1 = sw128_desc(smem_u32(q_s + C::kQBytes), 16, 1024);
+      int e = 0;  // ring entry of K_j
+      for (int j = lo; j <= hi && ok; ++j) {
+        const bool have_v = j > lo;
+        const bool have_k = j < hi;
+        const int ev = e - 1, ek = e;  // V_{j-1} precedes K_j in the ring
+        if (have_v)
+          ok = __all_sync(kFull, mbar_wait(&ctl->kv_full[ev % STAGES], (ev / STAGES) & 1, wc));
+        if (have_k && ok)
+          ok = __all_sync(kFull, mbar_wait(&ctl->kv_full[ek % STAGES], (ek / STAGES) & 1, wc));
+        if (!ok) break;
+        tc_fence_after();
+        // V panel: 128 keys x 64 columns; a K step of 16 keys is 2048 bytes; the next
+        // 64-column panel (N direction) is kChunkBytes further (LBO), 8-key groups are 1024
+        // bytes apart (SBO). K is K-major like Q.
+        const uint64_t v_desc =
+            sw128_desc(smem_u32(kv_s + (ev % STAGES) * C::kKVBytes), C::kChunkBytes, 1024);
+        const uint64_t k_desc = sw128_desc(smem_u32(kv_s + (ek % STAGES) * C::kKVBytes), 16, 1024);
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
           if (!ok) break;
-          tc_fence_after();
-          const uint32_t v_addr = smem_u32(kv_s + (ev % STAGES) * C::kKVBytes);
-          const uint32_t k_addr = smem_u32(kv_s + (ek % STAGES) * C::kKVBytes);
-          for (int i = 0; i < 2 && ok; ++i) {
-            if (have_v && active(i, j - 1)) {
-              ok = mbar_wait(&ctl->p_ready[i], (j - 1 - rng[i].lo) & 1, wc);
-              if (!ok) break;
-              tc_fence_after();
-              const uint32_t d_o = tmem + 256 + i * D;
-              const uint32_t a_p = tmem + i * 128;
+          if (have_v && active(i, j - 1)) {
+            ok = __all_sync(kFull, mbar_wait(&ctl->p_ready[i], (j - 1 - rng[i].lo) & 1, wc));
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t d_o = tmem + 256 + i * D;
+            const uint32_t a_p = tmem + i * 128;
+            const uint32_t acc0 = j - 1 > rng[i].lo ? 1u : 0u;
 #pragma unroll
-              for (int kk = 0; kk < BN / 16; ++kk) {
-                // V panel: 128 keys x 64 columns; K step = 16 keys = 2048 bytes; the next
-                // 64-column panel (N direction) is kChunkBytes further (LBO), 8-key groups
-                // are 1024 bytes apart (SBO).
-                const uint64_t bdesc = sw128_desc(v_addr + kk * 2048, C::kChunkBytes, 1024);
-                mma_ts(d_o, a_p + kk * 8, bdesc, C::kIdescO,
-                       (j - 1 > rng[i].lo || kk > 0) ? 1u : 0u);
-              }
-              if (j == rng[i].hi) mma_commit(&ctl->o_done[i]);
-              // Release V_{j-1} as soon as its last reader is issued.
-              if (i == 1 || !active(1, j - 1)) mma_commit(&ctl->kv_empty[ev % STAGES]);
-            }
-            if (have_k && active(i, j)) {
-              const uint32_t d_s = tmem + i * 128;
-#pragma unroll
-              for (int kk = 0; kk < D / 16; ++kk) {
-                // K-major panels: 16-column K step = 32 bytes inside a 128-byte swizzle row;
-                // every 4 steps move to the next 64-column panel. 8-row groups: 1024 bytes.
-                const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
-                mma_ss(d_s, sw128_desc(q_addr[i] + off, 16, 1024),
-                       sw128_desc(k_addr + off, 16, 1024), C::kIdescS, kk > 0 ? 1u : 0u);
-              }
-              mma_commit(&ctl->s_ready[i]);
-            }
+            for (int kk = 0; kk < BN / 16; ++kk)
+              mma_ts(d_o, a_p + kk * 8, v_desc + kk * (2048 >> 4), C::kIdescO,
+                     kk > 0 ? 1u : acc0);
+            if (j == rng[i].hi) mma_commit(&ctl->o_done[i]);
+            // Release V_{j-1} as soon as its last reader is issued.
+            if (i == 1 || !active(1, j - 1)) mma_commit(&ctl->kv_empty[ev % STAGES]);
           }
-          if (!ok) break;
-          if (have_k) mma_commit(&ctl->kv_empty[ek % STAGES]);
-          e += 2;
+          if (have_k && active(i, j)) {
+            const uint32_t d_s = tmem + i * 128;
+            const uint64_t q_desc = i ? q_desc1 : q_desc0;
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              // K-major panels: a 16-column K step is 32 bytes inside a 128-byte swizzle row;
+              // every 4 steps move to the next 64-column panel. 8-row groups: 1024 bytes.
+              const uint32_t off16 = ((kk >> 2) * C::kChunkBytes + (kk & 3) * 32) >> 4;
+              mma_ss(d_s, q_desc + off16, k_desc + off16, C::kIdescS, kk > 0 ? 1u : 0u);
+            }
+            mma_commit(&ctl->s_ready[i]);
+          }
         }
-        // Every MMA this thread issued has completed before TMEM can be released.
-        mma_commit(&ctl->drain);
-        mbar_wait(&ctl->drain, 0, wc_drain);
+        if (!ok) break;
+        if (have_k) mma_commit(&ctl->kv_empty[ek % STAGES]);
+        e += 2;
       }
+      // Every MMA this warp issued has completed before TMEM can be released.
+      mma_commit(&ctl->drain);
+      mbar_wait(&ctl->drain, 0, wc_drain);
       }
     } else {
       regs_increase<C::kRegsSoftmax>();
