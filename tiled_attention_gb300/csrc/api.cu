@@ -47,6 +47,23 @@ constexpr int kMaxDevices = 64;
 int* g_status_ptr[kMaxDevices];
 std::mutex g_mu;
 
+int g_num_sms[kMaxDevices];
+
+int sm_count(int* out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(ATTN_ERR_UNSUPPORTED, "device %d", dev);
+  if (!g_num_sms[dev]) {
+    int n = 0;
+    e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+    g_num_sms[dev] = n;
+  }
+  *out = g_num_sms[dev];
+  return ATTN_OK;
+}
+
 int status_ptr(int** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -288,8 +305,8 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
     return ATTN_OK;
   }
 
-  // Prefill kinds. DOCUMENT grids are an upper bound on the units (the segment lengths live
-  // on the device); surplus CTAs exit at once.
+  // Prefill kinds. For DOCUMENT the unit count is an upper bound (the segment lengths live
+  // on the device): units past the real end decode invalid and end a CTA's loop.
   const int planes_q = mask_kind == ATTN_MASK_DOCUMENT ? Hq : B * Hq;
   const int planes_kv = mask_kind == ATTN_MASK_DOCUMENT ? Hkv : B * Hkv;
   const long long units = mask_kind == ATTN_MASK_DOCUMENT
@@ -314,8 +331,12 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
   p.scale_log2 = scale * kLog2e;
   p.status = status;
   p.timeout_ns = kTimeoutNs;
-  cudaError_t e = d == 64 ? launch_prefill_d64(mask_kind, tq, tk, tv, to, p, p.num_units, stream)
-                          : launch_prefill_d128(mask_kind, tq, tk, tv, to, p, p.num_units, stream);
+  // Persistent: at most one CTA per SM (the kernel needs a whole SM's shared memory).
+  int sms = 0;
+  if ((rc = sm_count(&sms))) return rc;
+  const int grid = p.num_units < sms ? p.num_units : sms;
+  cudaError_t e = d == 64 ? launch_prefill_d64(mask_kind, tq, tk, tv, to, p, grid, stream)
+                          : launch_prefill_d128(mask_kind, tq, tk, tv, to, p, grid, stream);
   if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
   return ATTN_OK;
 }

@@ -1,8 +1,13 @@
 // prefill.cuh — fused tiled attention forward for sm_103a (dense, causal, sliding window,
 // document segments).
 //
-// One CTA computes one work unit: two 128-row query tiles of one (batch or segment, query
-// head). The tiled computation with a running row max m and row sum l, rescaling the output
+// Work unit: two 128-row query tiles of one (batch or segment, query head). The kernel is
+// persistent, one CTA per SM: CTA b of G takes units b, 2G-1-b, 2G+b, 4G-1-b, ... of the
+// longest-first unit list (a snake over rounds, which evens out the per-SM sums). The K/V ring,
+// three rotating Q buffers and every barrier phase run on across units, so the next unit's
+// loads and first S MMAs overlap the current unit's last tiles and epilogue.
+//
+// The tiled computation with a running row max m and row sum l, rescaling the output
 // accumulator by exp(m - m_new) when the max grows, is the one described in "Flash MSA
 // Attention Kernel Implementation Tutorial" ("Understanding Flash MSA Core Mechanics"); the
 // producer / consumer split with arrive / wait barriers around a double-use shared-memory
@@ -11,7 +16,8 @@
 // Blackwell: tcgen05 MMAs with accumulators in tensor memory instead of register WGMMA.
 //
 // Roles (384 threads):
-//   warp 0      TMA producer: Q tiles once, then K_j, V_j into a STAGES-deep smem ring.
+//   warp 0      TMA producer: per unit, the two Q tiles into the next free Q buffers, then
+//               K_j, V_j into a STAGES-deep smem ring.
 //   warp 1      MMA issuer (one elected lane) and TMEM owner: S_i = Q_i K_j^T (SS MMA) and
 //               O_i += P_i V_j (P read from TMEM, V from smem).
 //   warps 4-7   softmax warpgroup for query tile 0; warps 8-11 for query tile 1. One thread
@@ -40,7 +46,7 @@ struct PrefillParams {
   float* lse;               // fp32 [planes, N]
   const int* cu_seqlens;    // DOCUMENT: [B+1]
   int B, Hq, Hkv, N, group; // N: rows per (batch, head) plane (T for DOCUMENT)
-  int num_units;            // grid size; DOCUMENT grids are an upper bound
+  int num_units;            // work units; DOCUMENT: an upper bound (surplus ones decode invalid)
   int window;
   float scale_log2;         // scale * log2(e)
   int* status;
@@ -58,9 +64,13 @@ struct PrefillCfg {
   static constexpr int kKVBytes = BN * D * 2;
   static constexpr int kSmemLimit = 232448;           // 227 KB opt-in maximum per block
   static constexpr int kCtrlBytes = 1024;
-  static constexpr int kStagesFit = (kSmemLimit - 1024 - kCtrlBytes - 2 * kQBytes) / kKVBytes;
+  // Three Q buffers for two query tiles: the next unit's tile loads into a buffer released a
+  // key tile or more earlier, so its latency hides behind the current unit's last tiles.
+  static constexpr int kQBufs = 3;
+  static constexpr int kStagesFit =
+      (kSmemLimit - 1024 - kCtrlBytes - kQBufs * kQBytes) / kKVBytes;
   static constexpr int kStages = kStagesFit > 8 ? 8 : kStagesFit;
-  static constexpr int kSmemBytes = 1024 + 2 * kQBytes + kStages * kKVBytes + kCtrlBytes;
+  static constexpr int kSmemBytes = 1024 + kQBufs * kQBytes + kStages * kKVBytes + kCtrlBytes;
   static constexpr int kTmemCols = 512;
   // Launch: 384 threads x 168 registers = 64512. Warpgroup 0 (producer, MMA, two idle warps)
   // drops to 88, the two softmax warpgroups rise to 208: 128*88 + 256*208 = 64512.
@@ -71,7 +81,8 @@ struct PrefillCfg {
 };
 
 struct PrefillCtrl {
-  uint64_t q_full[2];
+  uint64_t q_full[3];
+  uint64_t q_empty[3];  // the epilogue that staged O in the buffer has finished with it
   uint64_t kv_full[8];
   uint64_t kv_empty[8];
   uint64_t s_ready[2];
@@ -80,7 +91,6 @@ struct PrefillCtrl {
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
-  int valid, bh, kvh, q_row0, k_org, k_end;
 };
 
 struct Unit {
@@ -190,32 +200,26 @@ __global__ void __launch_bounds__(384, 1)
                    const __grid_constant__ CUtensorMap tm_v,
                    const __grid_constant__ CUtensorMap tm_o, const PrefillParams p) {
   using C = PrefillCfg<D>;
-  constexpr int BM = C::BM, BN = C::BN, STAGES = C::kStages;
+  constexpr int BM = C::BM, BN = C::BN, STAGES = C::kStages, QB = C::kQBufs;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint8_t* q_s = smem;                                  // [2][kQBytes]
-  uint8_t* kv_s = smem + 2 * C::kQBytes;                // [STAGES][kKVBytes]
+  uint8_t* q_s = smem;                                  // [QB][kQBytes]
+  uint8_t* kv_s = smem + QB * C::kQBytes;               // [STAGES][kKVBytes]
   PrefillCtrl* ctl = reinterpret_cast<PrefillCtrl*>(kv_s + STAGES * C::kKVBytes);
+  static_assert(sizeof(PrefillCtrl) <= C::kCtrlBytes, "control block");
 
   const int warp = static_cast<int>(threadIdx.x >> 5);
   const int lane = static_cast<int>(lane_id());
 
-  // Loads issued before the block-wide barrier: the unit's Q tiles and the first STAGES ring
-  // entries (all slots start empty), so they are in flight while TMEM is allocated.
-  int e_early = 0;
   if (warp == 0) {
-    const Unit u = decode_unit<MASK>(static_cast<int>(blockIdx.x), p);
     if (lane == 0) {
-      ctl->valid = u.valid;
-      ctl->bh = u.bh;
-      ctl->kvh = u.kvh;
-      ctl->q_row0 = u.q_row0;
-      ctl->k_org = u.k_org;
-      ctl->k_end = u.k_end;
       ctl->abort_flag = 0;
+      for (int q = 0; q < QB; ++q) {
+        mbar_init(&ctl->q_full[q], 1);
+        mbar_init(&ctl->q_empty[q], 4);  // one arrival per epilogue warp
+      }
       for (int i = 0; i < 2; ++i) {
-        mbar_init(&ctl->q_full[i], 1);
         mbar_init(&ctl->s_ready[i], 1);
         mbar_init(&ctl->p_ready[i], 128);
         mbar_init(&ctl->o_done[i], 1);
@@ -226,30 +230,10 @@ __global__ void __launch_bounds__(384, 1)
       }
       mbar_init(&ctl->drain, 1);
       fence_mbar_init();
-      if (u.valid) {
-        prefetch_tensormap(&tm_q);
-        prefetch_tensormap(&tm_k);
-        prefetch_tensormap(&tm_v);
-        int lo = 0x7fffffff, hi = -1;
-        for (int i = 0; i < 2; ++i) {
-          const KvRange rg = kv_tile_range(MASK, p.window, u.q_row0 + i * BM, BM, u.k_end,
-                                           u.k_org, u.k_end, BN);
-          if (rg.hi <= rg.lo) continue;
-          lo = imin(lo, rg.lo);
-          hi = imax(hi, rg.hi);
-          mbar_arrive_expect_tx(&ctl->q_full[i], C::kQBytes);
-          for (int c = 0; c < C::kPanels; ++c)
-            tma_load_3d(q_s + i * C::kQBytes + c * C::kChunkBytes, &tm_q, &ctl->q_full[i], c * 64,
-                        u.q_row0 + i * BM, u.bh);
-        }
-        for (; e_early < STAGES && e_early < 2 * (hi - lo); ++e_early) {
-          mbar_arrive_expect_tx(&ctl->kv_full[e_early], C::kKVBytes);
-          const CUtensorMap* m = (e_early & 1) ? &tm_v : &tm_k;
-          for (int c = 0; c < C::kPanels; ++c)
-            tma_load_3d(kv_s + e_early * C::kKVBytes + c * C::kChunkBytes, m,
-                        &ctl->kv_full[e_early], c * 64, u.k_org + (lo + e_early / 2) * BN, u.kvh);
-        }
-      }
+      prefetch_tensormap(&tm_q);
+      prefetch_tensormap(&tm_k);
+      prefetch_tensormap(&tm_v);
+      prefetch_tensormap(&tm_o);
     }
   } else if (warp == 1) {
     tmem_alloc(&ctl->tmem_base, C::kTmemCols);
@@ -262,129 +246,202 @@ __global__ void __launch_bounds__(384, 1)
   const uint32_t tmem = ctl->tmem_base;
   const WaitCtl wc{p.timeout_ns, p.status, &ctl->abort_flag};
   const WaitCtl wc_drain{p.timeout_ns, p.status, nullptr};
-
-  if (ctl->valid) {
-    const int bh = ctl->bh, kvh = ctl->kvh, q_row0 = ctl->q_row0;
-    const int k_org = ctl->k_org, k_end = ctl->k_end;
-    const int row_end = k_end;  // query rows and keys share one index space
-    KvRange rng[2];
-    int lo = 0x7fffffff, hi = -1;
+  const int G = static_cast<int>(gridDim.x), b = static_cast<int>(blockIdx.x);
+  // The unit of this CTA's k-th round: a snake over the longest-first list.
+  auto unit_of = [&](int k) { return k * G + ((k & 1) ? G - 1 - b : b); };
+  // Key-tile ranges of a unit's two query tiles and their union [lo, hi). The two ranges
+  // overlap for every mask kind, so the union has no gap.
+  auto geometry = [&](const Unit& un, KvRange (&rng)[2], int& lo, int& hi) {
+    lo = 0x7fffffff;
+    hi = -1;
+#pragma unroll
     for (int i = 0; i < 2; ++i) {
-      rng[i] = kv_tile_range(MASK, p.window, q_row0 + i * BM, BM, row_end, k_org, k_end, BN);
+      rng[i] = kv_tile_range(MASK, p.window, un.q_row0 + i * BM, BM, un.k_end, un.k_org,
+                             un.k_end, BN);
       if (rng[i].hi > rng[i].lo) {
         lo = imin(lo, rng[i].lo);
         hi = imax(hi, rng[i].hi);
       }
     }
-    auto active = [&](int i, int j) { return j >= rng[i].lo && j < rng[i].hi; };
-    if (warp < 4) {
-      regs_decrease<C::kRegsControl>();
-      if (warp == 0) {
-      // ------------------------------------------------------------ TMA producer
-      if (lane == 0) {
-        // Ring entry e holds K_{lo + e/2} (e even) or V_{lo + e/2} (e odd).
-        int e = e_early;
-        bool ok = true;
-        for (; e < 2 * (hi - lo) && ok; ++e) {
-          const int st = e % STAGES;
-          ok = mbar_wait(&ctl->kv_empty[st], ((e / STAGES) & 1) ^ 1, wc);
-          if (!ok) break;
-          mbar_arrive_expect_tx(&ctl->kv_full[st], C::kKVBytes);
-          const CUtensorMap* m = (e & 1) ? &tm_v : &tm_k;
-          for (int c = 0; c < C::kPanels; ++c)
-            tma_load_3d(kv_s + st * C::kKVBytes + c * C::kChunkBytes, m, &ctl->kv_full[st],
-                        c * 64, k_org + (lo + e / 2) * BN, kvh);
+  };
+  // Every role walks the same unit sequence; a Q load is counted only for a query tile with
+  // work, in tile order, so all roles agree on which buffer (count % QB) holds which tile.
+
+  if (warp < 4) {
+    regs_decrease<C::kRegsControl>();
+    if (warp == 0) {
+      // -------------------------------------------------------------- TMA producer
+      int e = 0;   // K/V ring entries issued
+      int qn = 0;  // Q loads issued
+      bool ok = true;
+      for (int k = 0; ok; ++k) {
+        const int u = unit_of(k);
+        if (u >= p.num_units) break;
+        const Unit un = decode_unit<MASK>(u, p);  // warp-collective
+        if (!un.valid) break;
+        KvRange rng[2];
+        int lo, hi;
+        geometry(un, rng, lo, hi);
+        if (lane == 0) {
+          for (int i = 0; i < 2 && ok; ++i) {
+            if (rng[i].hi <= rng[i].lo) continue;
+            const int qb = qn % QB;
+            ok = mbar_wait(&ctl->q_empty[qb], ((qn / QB) & 1) ^ 1, wc);
+            if (!ok) break;
+            ++qn;
+            mbar_arrive_expect_tx(&ctl->q_full[qb], C::kQBytes);
+            for (int c = 0; c < C::kPanels; ++c)
+              tma_load_3d(q_s + qb * C::kQBytes + c * C::kChunkBytes, &tm_q, &ctl->q_full[qb],
+                          c * 64, un.q_row0 + i * BM, un.bh);
+          }
+          // Ring entry e holds K_{lo + x/2} (x = e - first entry of the unit, even) or V.
+          for (int x = 0; x < 2 * (hi - lo) && ok; ++x, ++e) {
+            const int st = e % STAGES;
+            ok = mbar_wait(&ctl->kv_empty[st], ((e / STAGES) & 1) ^ 1, wc);
+            if (!ok) break;
+            mbar_arrive_expect_tx(&ctl->kv_full[st], C::kKVBytes);
+            const CUtensorMap* m = (x & 1) ? &tm_v : &tm_k;
+            for (int c = 0; c < C::kPanels; ++c)
+              tma_load_3d(kv_s + st * C::kKVBytes + c * C::kChunkBytes, m, &ctl->kv_full[st],
+                          c * 64, un.k_org + (lo + x / 2) * BN, un.kvh);
+          }
         }
-        // Let copies still in flight land before the CTA can exit (no-op on the normal path).
-        for (int k = imax(0, e - STAGES); k < e; ++k)
-          mbar_wait(&ctl->kv_full[k % STAGES], (k / STAGES) & 1, wc_drain);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
       }
-      } else if (warp == 1) {
-      // ------------------------------------------------------------ MMA issuer
+      if (lane == 0) {
+        // Let copies still in flight land before the CTA can exit (no-op on the normal path).
+        for (int x = imax(0, e - STAGES); x < e; ++x)
+          mbar_wait(&ctl->kv_full[x % STAGES], (x / STAGES) & 1, wc_drain);
+        for (int x = imax(0, qn - QB); x < qn; ++x)
+          mbar_wait(&ctl->q_full[x % QB], (x / QB) & 1, wc_drain);
+      }
+    } else if (warp == 1) {
+      // -------------------------------------------------------------- MMA issuer
       // The whole warp runs this loop, so descriptors and loop state are warp-uniform; one
       // elected lane issues each tcgen05 instruction (see mma_ss). Waits are agreed on by the
       // whole warp so it never diverges.
       constexpr unsigned kFull = 0xffffffffu;
+      int e = 0;              // ring entry of the next K
+      int qc = 0;             // Q loads consumed before this unit
+      int pb0 = 0, pb1 = 0;   // P tiles consumed before this unit, per query tile
       bool ok = true;
-      if (rng[0].hi > rng[0].lo) ok = __all_sync(kFull, mbar_wait(&ctl->q_full[0], 0, wc));
-      if (ok && rng[1].hi > rng[1].lo) ok = __all_sync(kFull, mbar_wait(&ctl->q_full[1], 0, wc));
-      // Descriptors of the two Q tiles; a K step adds its byte offset / 16 to the start field,
-      // which stays inside its 14 bits for any shared-memory address.
-      const uint64_t q_desc0 = sw128_desc(smem_u32(q_s), 16, 1024);
-      const uint64_t q_desc1 = sw128_desc(smem_u32(q_s + C::kQBytes), 16, 1024);
-      int e = 0;  // ring entry of K_j
-      for (int j = lo; j <= hi && ok; ++j) {
-        const bool have_v = j > lo;
-        const bool have_k = j < hi;
-        const int ev = e - 1, ek = e;  // V_{j-1} precedes K_j in the ring
-        if (have_v)
-          ok = __all_sync(kFull, mbar_wait(&ctl->kv_full[ev % STAGES], (ev / STAGES) & 1, wc));
-        if (have_k && ok)
-          ok = __all_sync(kFull, mbar_wait(&ctl->kv_full[ek % STAGES], (ek / STAGES) & 1, wc));
-        if (!ok) break;
-        tc_fence_after();
-        // V panel: 128 keys x 64 columns; a K step of 16 keys is 2048 bytes; the next
-        // 64-column panel (N direction) is kChunkBytes further (LBO), 8-key groups are 1024
-        // bytes apart (SBO). K is K-major like Q.
-        const uint64_t v_desc =
-            sw128_desc(smem_u32(kv_s + (ev % STAGES) * C::kKVBytes), C::kChunkBytes, 1024);
-        const uint64_t k_desc = sw128_desc(smem_u32(kv_s + (ek % STAGES) * C::kKVBytes), 16, 1024);
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
+      for (int k = 0; ok; ++k) {
+        const int u = unit_of(k);
+        if (u >= p.num_units) break;
+        const Unit un = decode_unit<MASK>(u, p);  // warp-collective
+        if (!un.valid) break;
+        KvRange rng[2];
+        int lo, hi;
+        geometry(un, rng, lo, hi);
+        auto active = [&](int i, int j) { return j >= rng[i].lo && j < rng[i].hi; };
+        const int qn0 = qc, qn1 = qc + (rng[0].hi > rng[0].lo ? 1 : 0);
+        // Descriptors of the two Q tiles; a K step adds its byte offset / 16 to the start
+        // field, which stays inside its 14 bits for any shared-memory address.
+        const uint64_t q_desc0 = sw128_desc(smem_u32(q_s + (qn0 % QB) * C::kQBytes), 16, 1024);
+        const uint64_t q_desc1 = sw128_desc(smem_u32(q_s + (qn1 % QB) * C::kQBytes), 16, 1024);
+        for (int j = lo; j <= hi && ok; ++j) {
+          const bool have_v = j > lo;
+          const bool have_k = j < hi;
+          const int ev = e - 1, ek = e;  // V_{j-1} precedes K_j in the ring
+          if (have_v)
+            ok = __all_sync(kFull, mbar_wait(&ctl->kv_full[ev % STAGES], (ev / STAGES) & 1, wc));
+          if (have_k && ok)
+            ok = __all_sync(kFull, mbar_wait(&ctl->kv_full[ek % STAGES], (ek / STAGES) & 1, wc));
           if (!ok) break;
-          if (have_v && active(i, j - 1)) {
-            ok = __all_sync(kFull, mbar_wait(&ctl->p_ready[i], (j - 1 - rng[i].lo) & 1, wc));
+          tc_fence_after();
+          // V panel: 128 keys x 64 columns; a K step of 16 keys is 2048 bytes; the next
+          // 64-column panel (N direction) is kChunkBytes further (LBO), 8-key groups are 1024
+          // bytes apart (SBO). K is K-major like Q.
+          const uint64_t v_desc =
+              sw128_desc(smem_u32(kv_s + (ev % STAGES) * C::kKVBytes), C::kChunkBytes, 1024);
+          const uint64_t k_desc =
+              sw128_desc(smem_u32(kv_s + (ek % STAGES) * C::kKVBytes), 16, 1024);
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
             if (!ok) break;
-            tc_fence_after();
-            const uint32_t d_o = tmem + 256 + i * D;
-            const uint32_t a_p = tmem + i * 128;
-            const uint32_t acc0 = j - 1 > rng[i].lo ? 1u : 0u;
+            if (have_v && active(i, j - 1)) {
+              // The unit's first P.V overwrites O_i. The previous unit's epilogue has read O_i
+              // out by then: the softmax threads publish this P only after it.
+              const int pn = (i ? pb1 : pb0) + (j - 1 - rng[i].lo);
+              ok = __all_sync(kFull, mbar_wait(&ctl->p_ready[i], pn & 1, wc));
+              if (!ok) break;
+              tc_fence_after();
+              const uint32_t d_o = tmem + 256 + i * D;
+              const uint32_t a_p = tmem + i * 128;
+              const uint32_t acc0 = j - 1 > rng[i].lo ? 1u : 0u;
 #pragma unroll
-            for (int kk = 0; kk < BN / 16; ++kk)
-              mma_ts(d_o, a_p + kk * 8, v_desc + kk * (2048 >> 4), C::kIdescO,
-                     kk > 0 ? 1u : acc0);
-            if (j == rng[i].hi) mma_commit(&ctl->o_done[i]);
-            // Release V_{j-1} as soon as its last reader is issued.
-            if (i == 1 || !active(1, j - 1)) mma_commit(&ctl->kv_empty[ev % STAGES]);
-          }
-          if (have_k && active(i, j)) {
-            const uint32_t d_s = tmem + i * 128;
-            const uint64_t q_desc = i ? q_desc1 : q_desc0;
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-              // K-major panels: a 16-column K step is 32 bytes inside a 128-byte swizzle row;
-              // every 4 steps move to the next 64-column panel. 8-row groups: 1024 bytes.
-              const uint32_t off16 = ((kk >> 2) * C::kChunkBytes + (kk & 3) * 32) >> 4;
-              mma_ss(d_s, q_desc + off16, k_desc + off16, C::kIdescS, kk > 0 ? 1u : 0u);
+              for (int kk = 0; kk < BN / 16; ++kk)
+                mma_ts(d_o, a_p + kk * 8, v_desc + kk * (2048 >> 4), C::kIdescO,
+                       kk > 0 ? 1u : acc0);
+              if (j == rng[i].hi) mma_commit(&ctl->o_done[i]);
+              // Release V_{j-1} as soon as its last reader is issued.
+              if (i == 1 || !active(1, j - 1)) mma_commit(&ctl->kv_empty[ev % STAGES]);
             }
-            mma_commit(&ctl->s_ready[i]);
+            if (have_k && active(i, j)) {
+              if (j == rng[i].lo) {
+                const int qn = i ? qn1 : qn0;
+                ok = __all_sync(kFull, mbar_wait(&ctl->q_full[qn % QB], (qn / QB) & 1, wc));
+                if (!ok) break;
+                tc_fence_after();
+              }
+              const uint32_t d_s = tmem + i * 128;
+              const uint64_t q_desc = i ? q_desc1 : q_desc0;
+#pragma unroll
+              for (int kk = 0; kk < D / 16; ++kk) {
+                // K-major panels: a 16-column K step is 32 bytes inside a 128-byte swizzle
+                // row; every 4 steps move to the next 64-column panel. 8-row groups: 1024 B.
+                const uint32_t off16 = ((kk >> 2) * C::kChunkBytes + (kk & 3) * 32) >> 4;
+                mma_ss(d_s, q_desc + off16, k_desc + off16, C::kIdescS, kk > 0 ? 1u : 0u);
+              }
+              mma_commit(&ctl->s_ready[i]);
+            }
+          }
+          if (!ok) break;
+          if (have_k) {
+            mma_commit(&ctl->kv_empty[ek % STAGES]);
+            e += 2;  // K_j and V_j; the pass j == hi only drains V_{hi-1}
           }
         }
-        if (!ok) break;
-        if (have_k) mma_commit(&ctl->kv_empty[ek % STAGES]);
-        e += 2;
+        qc = qn1 + (rng[1].hi > rng[1].lo ? 1 : 0);
+        pb0 += imax(rng[0].hi - rng[0].lo, 0);
+        pb1 += imax(rng[1].hi - rng[1].lo, 0);
       }
       // Every MMA this warp issued has completed before TMEM can be released.
       mma_commit(&ctl->drain);
       mbar_wait(&ctl->drain, 0, wc_drain);
-      }
-    } else {
-      regs_increase<C::kRegsSoftmax>();
-      // ------------------------------------------------------------ softmax warpgroups
-      const int i = (warp - 4) >> 2;          // query tile
-      const int quarter = warp & 3;           // TMEM lanes [32*quarter, 32*quarter + 32)
-      const int r = quarter * 32 + lane;      // row inside the tile
-      const int row = q_row0 + i * BM + r;    // absolute query row
-      const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-      const uint32_t s_col = lane_base + i * 128;
-      const uint32_t o_col = lane_base + 256 + i * D;
-      const float c = p.scale_log2;
+    }
+  } else {
+    regs_increase<C::kRegsSoftmax>();
+    // ---------------------------------------------------------------- softmax warpgroups
+    const int i = (warp - 4) >> 2;          // query tile
+    const int quarter = warp & 3;           // TMEM lanes [32*quarter, 32*quarter + 32)
+    const int r = quarter * 32 + lane;      // row inside the tile
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const uint32_t s_col = lane_base + i * 128;
+    const uint32_t o_col = lane_base + 256 + i * D;
+    const float c = p.scale_log2;
+    int sc = 0, oc = 0;  // S tiles and finished units of this query tile consumed
+    int qc = 0;          // Q loads of all tiles before this unit
+    bool ok = true;
+    for (int k = 0; ok; ++k) {
+      const int u = unit_of(k);
+      if (u >= p.num_units) break;
+      const Unit un = decode_unit<MASK>(u, p);  // warp-collective
+      if (!un.valid) break;
+      KvRange rng[2];
+      int lo_u, hi_u;
+      geometry(un, rng, lo_u, hi_u);
       const KvRange my = i ? rng[1] : rng[0];
+      const int qn = qc + ((i == 1 && rng[0].hi > rng[0].lo) ? 1 : 0);  // this tile's Q load
+      qc += (rng[0].hi > rng[0].lo ? 1 : 0) + (rng[1].hi > rng[1].lo ? 1 : 0);
+      if (my.hi <= my.lo) continue;
+      const int q_row0 = un.q_row0, k_org = un.k_org, k_end = un.k_end, bh = un.bh;
+      const int row_end = k_end;  // query rows and keys share one index space
+      const int row = q_row0 + i * BM + r;  // absolute query row
       float m_run = -INFINITY;  // running max in log2 units (may trail the true max by < 8)
       float l_run = 0.f;
-      bool ok = true;
       for (int j = my.lo; j < my.hi && ok; ++j) {
-        ok = __all_sync(0xffffffffu, mbar_wait(&ctl->s_ready[i], (j - my.lo) & 1, wc));
+        ok = __all_sync(0xffffffffu, mbar_wait(&ctl->s_ready[i], (sc++) & 1, wc));
         if (!ok) break;
         tc_fence_after();
         uint32_t s0[32], s1[32], s2[32], s3[32];
@@ -435,93 +492,97 @@ __global__ void __launch_bounds__(384, 1)
           m_run = m_tile;
         }
         if (j > my.lo && __any_sync(0xffffffffu, alpha < 1.f)) {
+          // 16 columns at a time: the 128 scores are still live here.
 #pragma unroll
-          for (int cc = 0; cc < D / 32; ++cc) {
-            uint32_t ov[32];
-            tmem_ld_x32(o_col + cc * 32, ov);
-            tmem_wait_ld_x32(ov);
+          for (int cc = 0; cc < D / 16; ++cc) {
+            uint32_t ov[16];
+            tmem_ld_x16(o_col + cc * 16, ov);
+            tmem_wait_ld_x16(ov);
 #pragma unroll
-            for (int t = 0; t < 32; ++t)
+            for (int t = 0; t < 16; ++t)
               ov[t] = __float_as_uint(__uint_as_float(ov[t]) * alpha);
-            tmem_st_x32(o_col + cc * 32, ov);
+            tmem_st_x16(o_col + cc * 16, ov);
           }
         }
         const float msub = (m_run == -INFINITY) ? 0.f : m_run;
         // p = exp2(c*s - m) two at a time: one packed FMA, two MUFU ex2, one packed add into
         // two independent partial sums, one bf16x2 pack.
-        const float2 cc = make_float2(c, c);
+        const float2 cc2 = make_float2(c, c);
         const float2 mm = make_float2(-msub, -msub);
         float2 sa = make_float2(0.f, 0.f), sb = make_float2(0.f, 0.f);
-        uint32_t pk[32];
-        exp2_pack_32(f0, cc, mm, sa, sb, pk);
-        exp2_pack_32(f1, cc, mm, sa, sb, pk + 16);
-        tmem_st_x32(s_col + 0, pk);
-        exp2_pack_32(f2, cc, mm, sa, sb, pk);
-        exp2_pack_32(f3, cc, mm, sa, sb, pk + 16);
-        tmem_st_x32(s_col + 32, pk);
+        uint32_t pk[16];
+        exp2_pack_32(f0, cc2, mm, sa, sb, pk);
+        tmem_st_x16(s_col + 0, pk);
+        exp2_pack_32(f1, cc2, mm, sa, sb, pk);
+        tmem_st_x16(s_col + 16, pk);
+        exp2_pack_32(f2, cc2, mm, sa, sb, pk);
+        tmem_st_x16(s_col + 32, pk);
+        exp2_pack_32(f3, cc2, mm, sa, sb, pk);
+        tmem_st_x16(s_col + 48, pk);
         l_run = l_run * alpha + ((sa.x + sa.y) + (sb.x + sb.y));
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(&ctl->p_ready[i]);
       }
-      // ------------------------------------------------------------ epilogue
-      if (ok && my.hi > my.lo) {
-        ok = __all_sync(0xffffffffu, mbar_wait(&ctl->o_done[i], 0, wc));
-        if (ok) {
-          tc_fence_after();
-          const bool live = row < row_end;
-          const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
-          // The warp's 32 rows go out through shared memory and one TMA store per 64-column
-          // panel, written into Q_i's buffer (dead: its last S MMA completed before o_done) in
-          // the 128-byte-swizzled layout the store expects. Rows past the tensor's extent are
-          // clipped by the store; a DOCUMENT warp whose rows run past its segment writes
-          // them one thread per row instead, so the next segment's rows stay untouched.
-          const int warp_row0 = q_row0 + i * BM + quarter * 32;
-          const bool staged = MASK != kMaskDocument || warp_row0 + 31 < row_end;
-          uint8_t* stage = q_s + i * C::kQBytes;
-          uint8_t* orow = static_cast<uint8_t*>(p.o) +
-                          (static_cast<size_t>(bh) * p.N + static_cast<size_t>(row)) * D * 2;
+      if (!ok) break;
+      // -------------------------------------------------------------- epilogue
+      ok = __all_sync(0xffffffffu, mbar_wait(&ctl->o_done[i], (oc++) & 1, wc));
+      if (!ok) break;
+      tc_fence_after();
+      const bool live = row < row_end;
+      const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
+      // The warp's 32 rows go out through shared memory and one TMA store per 64-column
+      // panel, staged in this tile's Q buffer (its last S MMA completed before o_done) in the
+      // 128-byte-swizzled layout the store expects; the buffer goes back to the producer once
+      // the stores have read it. Rows past the tensor's extent are clipped by the store; a
+      // DOCUMENT warp whose rows run past its segment writes them one thread per row instead,
+      // so the next segment's rows stay untouched.
+      const int warp_row0 = q_row0 + i * BM + quarter * 32;
+      const bool staged = MASK != kMaskDocument || warp_row0 + 31 < row_end;
+      uint8_t* stage = q_s + (qn % QB) * C::kQBytes;
+      uint8_t* orow = static_cast<uint8_t*>(p.o) +
+                      (static_cast<size_t>(bh) * p.N + static_cast<size_t>(row)) * D * 2;
 #pragma unroll
-          for (int cc = 0; cc < D / 32; ++cc) {
-            uint32_t ov[32];
-            tmem_ld_x32(o_col + cc * 32, ov);
-            tmem_wait_ld_x32(ov);
-            uint32_t w[16];
+      for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t ov[32];
+        tmem_ld_x32(o_col + cc * 32, ov);
+        tmem_wait_ld_x32(ov);
+        uint32_t w[16];
 #pragma unroll
-            for (int t = 0; t < 16; ++t)
-              w[t] = pack_bf16x2(__uint_as_float(ov[2 * t]) * inv_l,
-                                 __uint_as_float(ov[2 * t + 1]) * inv_l);
-            if (staged) {
-              // 16-byte chunk k of row r sits at chunk k ^ (r % 8) of the row's 128 bytes.
-              const uint32_t rbase = smem_u32(stage + (cc >> 1) * C::kChunkBytes + r * 128);
+        for (int t = 0; t < 16; ++t)
+          w[t] = pack_bf16x2(__uint_as_float(ov[2 * t]) * inv_l,
+                             __uint_as_float(ov[2 * t + 1]) * inv_l);
+        if (staged) {
+          // 16-byte chunk k of row r sits at chunk k ^ (r % 8) of the row's 128 bytes.
+          const uint32_t rbase = smem_u32(stage + (cc >> 1) * C::kChunkBytes + r * 128);
 #pragma unroll
-              for (int v4 = 0; v4 < 4; ++v4)
-                st_shared_v4(rbase + ((((cc & 1) * 4 + v4) ^ (r & 7)) << 4), w[4 * v4],
-                             w[4 * v4 + 1], w[4 * v4 + 2], w[4 * v4 + 3]);
-            } else if (live) {
+          for (int v4 = 0; v4 < 4; ++v4)
+            st_shared_v4(rbase + ((((cc & 1) * 4 + v4) ^ (r & 7)) << 4), w[4 * v4],
+                         w[4 * v4 + 1], w[4 * v4 + 2], w[4 * v4 + 3]);
+        } else if (live) {
 #pragma unroll
-              for (int v4 = 0; v4 < 4; ++v4)
-                st_global_v4(orow + cc * 64 + v4 * 16, w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2],
-                             w[4 * v4 + 3]);
-            }
-          }
-          if (staged && warp_row0 < row_end) {
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-              for (int c = 0; c < C::kPanels; ++c)
-                tma_store_3d(&tm_o, stage + c * C::kChunkBytes + quarter * 32 * 128, c * 64,
-                             warp_row0, bh);
-              bulk_commit_group();
-              // The buffer must stay valid until the stores have read it.
-              bulk_wait_group_read0();
-            }
-          }
-          if (live)
-            p.lse[static_cast<size_t>(bh) * p.N + row] =
-                l_run > 0.f ? (m_run + log2f(l_run)) * 0.69314718055994530942f : -INFINITY;
+          for (int v4 = 0; v4 < 4; ++v4)
+            st_global_v4(orow + cc * 64 + v4 * 16, w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2],
+                         w[4 * v4 + 3]);
         }
       }
+      if (staged && warp_row0 < row_end) {
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          for (int cp = 0; cp < C::kPanels; ++cp)
+            tma_store_3d(&tm_o, stage + cp * C::kChunkBytes + quarter * 32 * 128, cp * 64,
+                         warp_row0, bh);
+          bulk_commit_group();
+          // The buffer is handed back only after the stores have read it.
+          bulk_wait_group_read0();
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl->q_empty[qn % QB]);
+      if (live)
+        p.lse[static_cast<size_t>(bh) * p.N + row] =
+            l_run > 0.f ? (m_run + log2f(l_run)) * 0.69314718055994530942f : -INFINITY;
     }
   }
 
