@@ -38,13 +38,18 @@ extern "C" {
  *  DOCUMENT      cu_seqlens[s] <= j <= i where segment s holds i (no attention across
  *                segments, causal inside one; same page, Pattern A).
  *  PAGED_DECODE  one query per sequence sees its whole context, read through a block table
- *                (same page, Pattern C). */
+ *                (same page, Pattern C).
+ *  DECODE        one query per sequence sees its whole context, read from a dense
+ *                per-sequence cache: the second stage ("standard attention kernel on the
+ *                gathered layout") of the two-stage paged path of the same page, Pattern C,
+ *                whose first stage is attn_gather_pages. */
 enum attn_mask_kind {
     ATTN_MASK_NONE = 0,
     ATTN_MASK_CAUSAL = 1,
     ATTN_MASK_SLIDING = 2,
     ATTN_MASK_DOCUMENT = 3,
-    ATTN_MASK_PAGED_DECODE = 4
+    ATTN_MASK_PAGED_DECODE = 4,
+    ATTN_MASK_DECODE = 5
 };
 
 enum attn_status {
@@ -62,27 +67,32 @@ enum attn_status {
  * attn_fwd — fused tiled attention forward pass.
  *
  * q, o      bf16. Dense kinds [B,Hq,N,d]; DOCUMENT [1,Hq,N,d] with N = total packed tokens;
- *           PAGED_DECODE [B,Hq,1,d].
+ *           PAGED_DECODE and DECODE [B,Hq,1,d].
  * k, v      bf16. Dense kinds [B,Hkv,N,d]; DOCUMENT [1,Hkv,N,d]; PAGED_DECODE page pools
- *           [num_pages,Hkv,page_size,d] (one (page, kv-head) block is contiguous).
+ *           [num_pages,Hkv,page_size,d] (one (page, kv-head) block is contiguous); DECODE
+ *           dense caches [B,Hkv,N,d] (rows past a sequence's length are never read into the
+ *           result).
  * lse       fp32, ln sum_j exp(scale * q_i . k_j) over the visible keys. [B,Hq,N]; DOCUMENT
- *           [1,Hq,N]; PAGED_DECODE [B,Hq].
+ *           [1,Hq,N]; PAGED_DECODE and DECODE [B,Hq].
  * B         batch (dense), number of segments (DOCUMENT) or sequences (PAGED_DECODE).
  * Hq, Hkv   query / key-value heads; Hq % Hkv == 0; query head h reads kv head h/(Hq/Hkv).
- * N         keys per sequence (dense), packed tokens (DOCUMENT), or the longest context
- *           (PAGED_DECODE: block_table has ceil(N/page_size) columns).
+ * N         keys per sequence (dense), packed tokens (DOCUMENT), the longest context
+ *           (PAGED_DECODE: block_table has ceil(N/page_size) columns), or the rows of each
+ *           dense cache (DECODE).
  * d         head dimension; 64 or 128 (else ATTN_ERR_UNSUPPORTED).
  * scale     multiplies q.k before the softmax (callers usually pass 1/sqrt(d)).
  * mask_kind enum attn_mask_kind.
  * window    SLIDING only: number of keys visible to a query (>= 1). Ignored otherwise.
  * cu_seqlens int32 device array [B+1], cu[0] = 0, nondecreasing. DOCUMENT: segment starts,
- *           cu[B] = N. PAGED_DECODE: cumulative context lengths (L_b = cu[b+1] - cu[b],
- *           0 <= L_b <= N). Checked on the device (status ATTN_ERR_SEQLENS). Unused otherwise.
+ *           cu[B] = N. PAGED_DECODE and DECODE: cumulative context lengths
+ *           (L_b = cu[b+1] - cu[b], 0 <= L_b <= N). Checked on the device (status
+ *           ATTN_ERR_SEQLENS). Unused otherwise.
  * block_table int32 device array [B, ceil(N/page_size)]: physical page of logical page p of
  *           sequence b; entries past a sequence's last page are ignored (-1 by convention).
  *           PAGED_DECODE only.
  * page_size tokens per page; PAGED_DECODE supports 64.
  * num_pages pages in the k / v pools (PAGED_DECODE; bounds-checked on the device).
+ *           block_table, page_size and num_pages are ignored for DECODE.
  * workspace device scratch of at least attn_workspace_bytes(...) bytes (may be NULL when that
  *           is 0). Its contents need not be initialised; concurrent calls need separate ones.
  * stream    cudaStream_t to launch on.
@@ -93,7 +103,8 @@ int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse, i
              const int32_t *cu_seqlens, const int32_t *block_table, int page_size,
              int num_pages, void *workspace, size_t workspace_bytes, void *stream);
 
-/* Bytes of workspace attn_fwd needs for these arguments (0 for the prefill kinds). */
+/* Bytes of workspace attn_fwd needs for these arguments (0 for the prefill kinds; DECODE
+ * ignores page_size). */
 size_t attn_workspace_bytes(int B, int Hq, int Hkv, int N, int d, int mask_kind, int page_size);
 
 /*

@@ -83,7 +83,7 @@ def attention(w, rows=None, probs: bool = False, threads: int = 0, lib_path: str
         n = rows_arr.size
     o = np.zeros((n, w.d), dtype=np.float64)
     lse = np.zeros(n, dtype=np.float64)
-    nk = w.N if w.mask_kind != 4 else int(np.diff(cu).max(initial=0))
+    nk = w.N if w.mask_kind not in (4, 5) else int(np.diff(cu).max(initial=0))
     pr = np.zeros((n, max(nk, 1)), dtype=np.float64) if probs else None
     rc = lib.oracle_attn(_ptr(q), _ptr(k), _ptr(v), w.B, w.Hq, w.Hkv, w.N, w.d,
                          ctypes.c_float(w.scale), w.mask_kind, w.window, _ptr(cu), _ptr(tab),

@@ -29,6 +29,9 @@
  *              segment; the segment-offset mask of the same page, Pattern A)
  *   PAGED      all j < L_b, key/value j of sequence b read from physical page
  *              table[b][j / page] at slot j % page (the block-table indirection of Pattern C)
+ *   DECODE     all j < L_b, key/value j of sequence b read from a dense per-sequence cache
+ *              k[b, g, j, :] (the "standard attention kernel on the gathered layout" that
+ *              is the second stage of Pattern C's two-stage path)
  *
  * Inputs are raw bf16 bit patterns widened exactly to fp64. The fp32 scale is widened too.
  * A row that sees no key (impossible for valid inputs) gets O = 0 and LSE = -inf.
@@ -41,7 +44,10 @@
 #include <omp.h>
 #endif
 
-enum { OR_NONE = 0, OR_CAUSAL = 1, OR_SLIDING = 2, OR_DOCUMENT = 3, OR_PAGED = 4 };
+enum { OR_NONE = 0, OR_CAUSAL = 1, OR_SLIDING = 2, OR_DOCUMENT = 3, OR_PAGED = 4, OR_DECODE = 5 };
+
+/* One query per sequence (PAGED, DECODE). */
+static int is_decode(int mask) { return mask == OR_PAGED || mask == OR_DECODE; }
 
 typedef struct {
     const uint16_t *q, *k, *v;
@@ -62,14 +68,14 @@ static double widen_bf16(uint16_t bits) {
 
 /* Number of query rows, in the flattened order of the O / LSE outputs. */
 static int64_t row_count(const problem_t *P) {
-    if (P->mask == OR_PAGED) return (int64_t)P->B * P->Hq;
+    if (is_decode(P->mask)) return (int64_t)P->B * P->Hq;
     if (P->mask == OR_DOCUMENT) return (int64_t)P->Hq * P->N;
     return (int64_t)P->B * P->Hq * P->N;
 }
 
 /* Flattened row r -> (b, h, i). For DOCUMENT, b is the segment that holds token i. */
 static void row_coords(const problem_t *P, int64_t r, int *b, int *h, int *i) {
-    if (P->mask == OR_PAGED) {
+    if (is_decode(P->mask)) {
         *b = (int)(r / P->Hq);
         *h = (int)(r % P->Hq);
         *i = 0;
@@ -88,7 +94,7 @@ static void row_coords(const problem_t *P, int64_t r, int *b, int *h, int *i) {
 
 /* Number of keys row i of batch b can address (before the mask). */
 static int key_count(const problem_t *P, int b) {
-    if (P->mask == OR_PAGED) return P->cu[b + 1] - P->cu[b];
+    if (is_decode(P->mask)) return P->cu[b + 1] - P->cu[b];
     return P->N;
 }
 
@@ -98,13 +104,14 @@ static int visible(const problem_t *P, int b, int i, int j) {
     case OR_CAUSAL: return j <= i;
     case OR_SLIDING: return j <= i && j > i - P->W;
     case OR_DOCUMENT: return j <= i && j >= P->cu[b];
-    case OR_PAGED: return j < P->cu[b + 1] - P->cu[b];
+    case OR_PAGED:
+    case OR_DECODE: return j < P->cu[b + 1] - P->cu[b];
     }
     return 0;
 }
 
 static const uint16_t *query_row(const problem_t *P, int b, int h, int i) {
-    if (P->mask == OR_PAGED) return P->q + ((size_t)b * P->Hq + h) * P->d;
+    if (is_decode(P->mask)) return P->q + ((size_t)b * P->Hq + h) * P->d;
     if (P->mask == OR_DOCUMENT) return P->q + ((size_t)h * P->N + i) * P->d;
     return P->q + (((size_t)b * P->Hq + h) * P->N + i) * P->d;
 }
@@ -177,17 +184,21 @@ int oracle_attn(const uint16_t *q, const uint16_t *k, const uint16_t *v, int B, 
     problem_t P = {q, k, v, B, Hq, Hkv, N, d, (double)scale, mask_kind, window,
                    cu_seqlens, block_table, max_pages, page_size};
     if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || d <= 0 || N < 0) return -1;
-    if (mask_kind < OR_NONE || mask_kind > OR_PAGED) return -1;
+    if (mask_kind < OR_NONE || mask_kind > OR_DECODE) return -1;
     if (mask_kind == OR_SLIDING && window < 1) return -1;
-    if ((mask_kind == OR_DOCUMENT || mask_kind == OR_PAGED) && !cu_seqlens) return -1;
+    if ((mask_kind == OR_DOCUMENT || is_decode(mask_kind)) && !cu_seqlens) return -1;
+    for (int b = 0; mask_kind == OR_DECODE && b < B; b++) {
+        const int L = cu_seqlens[b + 1] - cu_seqlens[b];
+        if (L < 0 || L > N) return -1;  /* the dense cache holds N keys per sequence */
+    }
     if (mask_kind == OR_PAGED && (!block_table || page_size <= 0)) return -1;
 
     const int64_t total = row_count(&P);
     const int64_t n = rows ? nrows : total;
     for (int64_t t = 0; rows && t < n; t++)
         if (rows[t] < 0 || rows[t] >= total) return -1;
-    int maxk = (mask_kind == OR_PAGED) ? 0 : N;
-    for (int b = 0; mask_kind == OR_PAGED && b < B; b++) {
+    int maxk = is_decode(mask_kind) ? 0 : N;
+    for (int b = 0; is_decode(mask_kind) && b < B; b++) {
         int L = cu_seqlens[b + 1] - cu_seqlens[b];
         if (L > maxk) maxk = L;
     }

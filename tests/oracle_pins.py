@@ -16,7 +16,7 @@ from tiled_attention_gb300 import inputs as I
 
 GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
 
-KINDS = ["none", "causal", "sliding", "document", "paged"]
+KINDS = ["none", "causal", "sliding", "document", "paged", "decode"]
 
 
 def widen(bits):
@@ -40,6 +40,8 @@ def tiny(kind: str, seed: int = 7, window: int = 5):
     if kind == "paged":
         return I.paged_decode_workload(seed, 3, 0, 0, 4, 2, 16, page_size=8, spare_pages=3,
                                        context_lens=[1, 63, 130])
+    if kind == "decode":
+        return I.dense_decode_workload(seed, 3, 0, 0, 4, 2, 16, N=137, context_lens=[1, 63, 130])
     raise KeyError(kind)
 
 
@@ -70,6 +72,13 @@ def dense_problems(w):
         for h in range(w.Hq):
             rows = h * T + np.arange(T)
             yield rows, qf[0, h], kf[0, h // group], vf[0, h // group], mask.numpy()
+    elif w.mask_kind == I.MASK_DECODE:
+        for b in range(w.B):
+            L = int(w.cu_seqlens[b + 1] - w.cu_seqlens[b])
+            for h in range(w.Hq):
+                g = h // group
+                yield (np.array([b * w.Hq + h]), qf[b, h], kf[b, g, :L], vf[b, g, :L],
+                       np.ones((1, L), dtype=bool))
     else:
         P = w.page_size
         for b in range(w.B):
@@ -152,6 +161,14 @@ def _set_dominant(w, r, jstar):
         w.k[:, g, :, 0] = 0
         P = w.page_size
         w.k[w.block_table[b, jstar // P], g, jstar % P, 0] = bf16(32.0)
+        return
+    if w.mask_kind == I.MASK_DECODE:
+        b, h = divmod(r, w.Hq)
+        g = h // group
+        w.q[b, h, 0, :] = 0
+        w.q[b, h, 0, 0] = bf16(32.0)
+        w.k[b, g, :, 0] = 0
+        w.k[b, g, jstar, 0] = bf16(32.0)
         return
     if w.mask_kind == I.MASK_DOCUMENT:
         h, i = divmod(r, w.N)
@@ -268,6 +285,8 @@ def pin_gqa_equals_repeated_mha(attn, kind):
         m = I.paged_decode_workload(7, 3, 0, 0, 4, 4, 16, page_size=8, spare_pages=3,
                                     context_lens=[1, 63, 130])
         m.block_table = w.block_table.copy()
+    elif kind == "decode":
+        m = I.dense_decode_workload(7, 3, 0, 0, 4, 4, 16, N=137, context_lens=[1, 63, 130])
     elif kind == "document":
         m = I.document_workload(7, 37, 4, 16, cu_seqlens=[0, 5, 6, 20, 37], Hkv=4)
     else:
@@ -327,6 +346,20 @@ def pin_online_recurrence(attn, kind):
             np.testing.assert_allclose(m + np.log(l), lse[rows], rtol=0, atol=1e-12)
 
 
+def pin_dense_decode_equals_paged(attn):
+    """A dense-cache decode and a paged decode drawn with the same arguments hold the same
+    keys in different places, so they give the same results bit for bit (each sums its keys
+    in key order)."""
+    for lens in ([1, 63, 130], [64, 65, 7, 300]):
+        d = I.dense_decode_workload(13, len(lens), 0, 0, 8, 2, 16, context_lens=lens)
+        pg = I.paged_decode_workload(13, len(lens), 0, 0, 8, 2, 16, page_size=8,
+                                     spare_pages=5, context_lens=lens)
+        od, ld = attn(d)
+        op, lp = attn(pg)
+        assert np.array_equal(od, op)
+        assert np.array_equal(ld, lp)
+
+
 def pin_closed_form_golden(attn):
     g = json.load(open(os.path.join(GOLDEN, "closed_form_2x2.json")))
     inp = g["inputs"]
@@ -352,6 +385,6 @@ def all_pins():
             pins.append((f"{f.__name__}[{kind}]", (lambda f, kind: lambda a: f(a, kind))(f, kind)))
     for f in (pin_key_permutation, pin_window_covering_equals_causal,
               pin_single_segment_equals_causal, pin_paged_equals_dense_last_row,
-              pin_closed_form_golden):
+              pin_dense_decode_equals_paged, pin_closed_form_golden):
         pins.append((f.__name__, f))
     return pins

@@ -47,6 +47,7 @@ def _call(**kw):
     (dict(scale=-1.0), attn.ATTN_ERR_UNSUPPORTED),
     (dict(mask_kind=SLIDING, window=0), attn.ATTN_ERR_INVALID),
     (dict(mask_kind=DOCUMENT), attn.ATTN_ERR_INVALID),
+    (dict(mask_kind=attn.ATTN_MASK_DECODE), attn.ATTN_ERR_INVALID),  # no cu_seqlens
     (dict(B=-1), attn.ATTN_ERR_INVALID),
     (dict(Hkv=0), attn.ATTN_ERR_INVALID),
 ])
@@ -64,11 +65,37 @@ def test_null_tensors_rejected():
     assert _call() == attn.ATTN_ERR_INVALID
 
 
+class _FakeDevicePtr:
+    """Stands in for a device tensor in calls that must fail validation before any CUDA
+    call: non-null and 16-byte aligned, never dereferenced."""
+
+    def __init__(self, addr=1 << 20):
+        self.addr = addr
+
+    def data_ptr(self):
+        return self.addr
+
+
+def test_decode_validation_before_cuda():
+    t = _FakeDevicePtr()
+    base = dict(q=t, k=t, v=t, o=t, lse=t, cu_seqlens=t, N=256)
+    # three query heads per kv head: no decode instantiation
+    assert _call(mask_kind=attn.ATTN_MASK_DECODE, Hq=3, Hkv=1, **base) == attn.ATTN_ERR_UNSUPPORTED
+    # workspace missing
+    assert (_call(mask_kind=attn.ATTN_MASK_DECODE, Hq=4, Hkv=1, **base)
+            == attn.ATTN_ERR_WORKSPACE)
+    # paged decode still needs its block table
+    assert (_call(mask_kind=attn.ATTN_MASK_PAGED_DECODE, Hq=4, Hkv=1, page_size=64,
+                  num_pages=4, **base) == attn.ATTN_ERR_INVALID)
+
+
 def test_workspace_bytes():
     assert attn.attn_workspace_bytes(4, 16, 16, 2048, 128, CAUSAL, 0) == 0
     n = attn.attn_workspace_bytes(32, 32, 8, 16384, 128, 4, 64)
     # partial O for 16 splits x 4 heads x 128 columns per (sequence, kv head), plus stats
     assert n >= 32 * 8 * 16 * 4 * 128 * 4
+    # the dense-cache decode splits the same way and ignores page_size
+    assert attn.attn_workspace_bytes(32, 32, 8, 16384, 128, attn.ATTN_MASK_DECODE, 0) == n
 
 
 # ---------------------------------------------------------------- tile scheduler

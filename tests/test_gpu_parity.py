@@ -139,6 +139,63 @@ def test_paged_ragged(d, group):
     compare(w, run(w), strict=False)
 
 
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("group", [1, 4, 16])
+def test_dense_decode_ragged(d, group):
+    """Decode on dense per-sequence caches; the cache is longer than every context and its
+    tail holds poison, so reading past L_b would show."""
+    lens = [1, 63, 64, 65, 1000, 1025, 2048, 3000]
+    w = I.dense_decode_workload(500 + group, len(lens), 0, 0, 2 * group, 2, d, N=3100,
+                                context_lens=lens)
+    compare(w, run(w), strict=False)
+
+
+def test_dense_decode_empty_context():
+    w = I.dense_decode_workload(9, 3, 0, 0, 8, 2, 128, N=100, context_lens=[0, 70, 0])
+    dp = run(w)
+    o, lse = dp.outputs()
+    ro, rl = oracle.attention(w)
+    assert np.abs(o - ro).max() <= O_TOL
+    assert np.array_equal(np.isinf(lse), np.isinf(rl))
+    live = np.isfinite(rl)
+    assert np.abs(lse[live] - rl[live]).max() <= LSE_TOL
+
+
+def test_two_stage_paged_equals_fused():
+    """Gather the pages into dense caches, then decode on them: the same pages in the same
+    order through the same kernel, so the result equals the fused paged decode bit for bit."""
+    lens = [1, 64, 65, 300, 1000, 4097]
+    w = I.paged_decode_workload(21, len(lens), 0, 0, 16, 4, 128, context_lens=lens)
+    fused = run(w)
+    max_pages = w.block_table.shape[1]
+    L = max_pages * 64
+    kd = torch.zeros((w.B, w.Hkv, L, w.d), dtype=torch.bfloat16, device="cuda")
+    vd = torch.zeros_like(kd)
+    for src, dst in ((fused.k, kd), (fused.v, vd)):
+        rc = attn.attn_gather_pages(src, dst, fused.table, w.B, max_pages, w.Hkv, 64, w.d,
+                                    fused.num_pages)
+        assert rc == 0, attn.last_error()
+    o = torch.full(w.out_shape, float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full(w.lse_shape, float("nan"), dtype=torch.float32, device="cuda")
+    nbytes = attn.attn_workspace_bytes(w.B, w.Hq, w.Hkv, L, w.d, attn.ATTN_MASK_DECODE, 0)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    rc = attn.attn_fwd(fused.q, kd, vd, o, lse, w.B, w.Hq, w.Hkv, L, w.d, w.scale,
+                       attn.ATTN_MASK_DECODE, 0, fused.cu, None, 0, 0, ws)
+    assert rc == 0, attn.last_error()
+    torch.cuda.synchronize()
+    assert attn.attn_get_status() == 0
+    assert torch.equal(o.view(torch.int16), fused.o.view(torch.int16))
+    assert torch.equal(lse, fused.lse)
+
+
+def test_dense_decode_length_past_cache_reports_status():
+    w = I.dense_decode_workload(23, 2, 0, 0, 4, 1, 64, N=128, context_lens=[100, 128])
+    w.cu_seqlens = np.array([0, 100, 229], dtype=np.int32)  # second length 129 > N
+    dp = DeviceProblem(w)
+    assert dp.run() == 0
+    assert attn.attn_get_status() == attn.ATTN_ERR_SEQLENS
+
+
 def test_paged_empty_context():
     w = I.paged_decode_workload(9, 3, 0, 0, 8, 2, 128, context_lens=[0, 70, 0])
     dp = run(w)

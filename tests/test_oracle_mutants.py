@@ -22,8 +22,8 @@ MUTANTS = [
     ("kv_batch_head_swapped", "return base + (((size_t)b * P->Hkv + g) * P->N + j) * P->d;",
      "return base + (((size_t)g * P->B + b) * P->N + j) * P->d;"),
     ("paged_slot", "(size_t)(j % P->page)) * P->d;", "(size_t)(j / P->page)) * P->d;"),
-    ("paged_length", "case OR_PAGED: return j < P->cu[b + 1] - P->cu[b];",
-     "case OR_PAGED: return j <= P->cu[b + 1] - P->cu[b] - 2;"),
+    ("paged_length", "case OR_DECODE: return j < P->cu[b + 1] - P->cu[b];",
+     "case OR_DECODE: return j <= P->cu[b + 1] - P->cu[b] - 2;"),
     ("scale_dropped", "z[j] = P->s * dot;", "z[j] = dot;"),
     ("max_not_subtracted_in_sum", "if (visible(P, b, i, j)) l += exp(z[j] - M);",
      "if (visible(P, b, i, j)) l += exp(z[j]);"),

@@ -19,6 +19,7 @@ ATTN_MASK_CAUSAL = 1
 ATTN_MASK_SLIDING = 2
 ATTN_MASK_DOCUMENT = 3
 ATTN_MASK_PAGED_DECODE = 4
+ATTN_MASK_DECODE = 5
 
 ATTN_OK = 0
 ATTN_ERR_INVALID = -1

@@ -119,6 +119,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 constexpr unsigned long long kTimeoutNs = 2000000000ull;  // 2 s per pipeline wait
 constexpr int kDecodeChunkPages = 16;
+constexpr int kDecodePage = 64;  // tokens per page (the pool's, or 64-row slices of a cache)
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct DecodeLayout {
@@ -216,8 +217,9 @@ const char* attn_last_error(void) { return g_last_error.c_str(); }
 
 size_t attn_workspace_bytes(int B, int Hq, int Hkv, int N, int d, int mask_kind,
                             int page_size) {
-  if (mask_kind != ATTN_MASK_PAGED_DECODE || B <= 0 || Hkv <= 0 || Hq <= 0 || N <= 0 ||
-      page_size <= 0 || d <= 0)
+  if (mask_kind == ATTN_MASK_DECODE) page_size = kDecodePage;
+  if ((mask_kind != ATTN_MASK_PAGED_DECODE && mask_kind != ATTN_MASK_DECODE) || B <= 0 ||
+      Hkv <= 0 || Hq <= 0 || N <= 0 || page_size <= 0 || d <= 0)
     return 0;
   return decode_layout(B, Hq, Hkv, N, d, page_size).total;
 }
@@ -228,8 +230,9 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
              int num_pages, void* workspace, size_t workspace_bytes, void* stream_) {
   g_last_error.clear();
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
-  if (mask_kind < ATTN_MASK_NONE || mask_kind > ATTN_MASK_PAGED_DECODE)
+  if (mask_kind < ATTN_MASK_NONE || mask_kind > ATTN_MASK_DECODE)
     return fail(ATTN_ERR_INVALID, "unknown mask_kind %d", mask_kind);
+  const bool decode = mask_kind == ATTN_MASK_PAGED_DECODE || mask_kind == ATTN_MASK_DECODE;
   if (B < 0 || N < 0 || Hq <= 0 || Hkv <= 0)
     return fail(ATTN_ERR_INVALID, "need B >= 0, N >= 0, Hq > 0, Hkv > 0");
   if (Hq % Hkv != 0) return fail(ATTN_ERR_INVALID, "Hq (%d) %% Hkv (%d) != 0", Hq, Hkv);
@@ -238,7 +241,7 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
   if (!(scale > 0.f)) return fail(ATTN_ERR_UNSUPPORTED, "scale must be > 0");
   if (mask_kind == ATTN_MASK_SLIDING && window < 1)
     return fail(ATTN_ERR_INVALID, "window %d < 1", window);
-  if ((mask_kind == ATTN_MASK_DOCUMENT || mask_kind == ATTN_MASK_PAGED_DECODE) && !cu_seqlens)
+  if ((mask_kind == ATTN_MASK_DOCUMENT || decode) && !cu_seqlens)
     return fail(ATTN_ERR_INVALID, "cu_seqlens is required");
   if (B == 0 || N == 0) return ATTN_OK;  // nothing to compute
   if (!q || !k || !v || !o || !lse) return fail(ATTN_ERR_INVALID, "null tensor pointer");
@@ -246,15 +249,20 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
     return fail(ATTN_ERR_INVALID, "tensors must be 16-byte aligned");
   const int group = Hq / Hkv;
   DecodeLayout L{};
-  if (mask_kind == ATTN_MASK_PAGED_DECODE) {
-    if (!block_table) return fail(ATTN_ERR_INVALID, "block_table is required");
-    if (page_size != 64) return fail(ATTN_ERR_UNSUPPORTED, "page_size %d (64)", page_size);
-    if (num_pages <= 0) return fail(ATTN_ERR_INVALID, "num_pages %d", num_pages);
+  if (decode) {
+    if (mask_kind == ATTN_MASK_PAGED_DECODE) {
+      if (!block_table) return fail(ATTN_ERR_INVALID, "block_table is required");
+      if (page_size != kDecodePage)
+        return fail(ATTN_ERR_UNSUPPORTED, "page_size %d (%d)", page_size, kDecodePage);
+      if (num_pages <= 0) return fail(ATTN_ERR_INVALID, "num_pages %d", num_pages);
+      if (static_cast<long long>(num_pages) * Hkv >= (1ll << 31))
+        return fail(ATTN_ERR_UNSUPPORTED, "page pool too large");
+    } else if (static_cast<long long>(B) * Hkv >= (1ll << 31)) {
+      return fail(ATTN_ERR_UNSUPPORTED, "B*Hkv too large");
+    }
     if (group != 1 && group != 2 && group != 4 && group != 8 && group != 16)
       return fail(ATTN_ERR_UNSUPPORTED, "query heads per kv head %d (1, 2, 4, 8, 16)", group);
-    if (static_cast<long long>(num_pages) * Hkv >= (1ll << 31))
-      return fail(ATTN_ERR_UNSUPPORTED, "page pool too large");
-    L = decode_layout(B, Hq, Hkv, N, d, page_size);
+    L = decode_layout(B, Hq, Hkv, N, d, kDecodePage);
     if (L.max_splits > 65535 || Hkv > 65535 || B > 65535)
       return fail(ATTN_ERR_UNSUPPORTED, "decode grid too large");
     if (!workspace || workspace_bytes < L.total || !aligned16(workspace))
@@ -271,17 +279,22 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
   int rc = status_ptr(&status);
   if (rc) return rc;
 
-  if (mask_kind == ATTN_MASK_PAGED_DECODE) {
+  if (decode) {
+    // PAGED_DECODE: the pools as [num_pages * Hkv][64][d]; DECODE: the dense caches as
+    // [B * Hkv][N][d]. Boxes of 64 rows: one page of one kv head.
+    const bool dense = mask_kind == ATTN_MASK_DECODE;
+    const uint64_t rows = dense ? static_cast<uint64_t>(N) : kDecodePage;
+    const uint64_t planes = dense ? static_cast<uint64_t>(B) * Hkv
+                                  : static_cast<uint64_t>(num_pages) * Hkv;
     CUtensorMap tk, tv;
-    if ((rc = encode_3d(&tk, k, d, page_size, static_cast<uint64_t>(num_pages) * Hkv, 64)))
-      return rc;
-    if ((rc = encode_3d(&tv, v, d, page_size, static_cast<uint64_t>(num_pages) * Hkv, 64)))
-      return rc;
+    if ((rc = encode_3d(&tk, k, d, rows, planes, kDecodePage))) return rc;
+    if ((rc = encode_3d(&tv, v, d, rows, planes, kDecodePage))) return rc;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     DecodeParams p{};
     p.q = static_cast<const uint4*>(q);
     p.cu = cu_seqlens;
-    p.table = block_table;
+    p.table = dense ? nullptr : block_table;
+    p.dense = dense ? 1 : 0;
     p.o = o;
     p.lse = lse;
     p.part_o = reinterpret_cast<float*>(ws + L.part_o);
@@ -291,7 +304,8 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
     p.Hq = Hq;
     p.Hkv = Hkv;
     p.max_pages = L.max_pages;
-    p.num_pages = num_pages;
+    p.num_pages = dense ? 0 : num_pages;
+    p.max_len = dense ? N : L.max_pages * kDecodePage;
     p.max_splits = L.max_splits;
     p.chunk_pages = kDecodeChunkPages;
     p.scale_log2 = scale * kLog2e;

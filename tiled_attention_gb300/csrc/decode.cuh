@@ -5,7 +5,9 @@
 // at physical page block_table[b][p] ("Optimizing Triton Kernels for Custom Attention
 // Patterns on H100", Pattern C). Instead of first gathering pages into a dense buffer, the
 // producer warp issues one TMA box per (page, kv-head, 64 columns) straight from the pool into
-// a shared-memory ring, so every K/V byte crosses HBM once.
+// a shared-memory ring, so every K/V byte crosses HBM once. The same kernel also reads dense
+// per-sequence caches [B, Hkv, L, D] (p.dense): the second stage of that page's two-stage
+// path, which first gathers the pages into such a cache.
 //
 // Grid (split, kv head g, sequence b): a CTA handles `chunk_pages` pages of one (b, g) for
 // all G = Hq/Hkv query heads of the group. Decode reads each K/V byte once and is HBM-bound;
@@ -41,6 +43,8 @@ struct DecodeParams {
   float* part_ml;        // [B*Hkv, max_splits, G, 2]
   int* counters;         // [B*Hkv], zero before the launch
   int B, Hq, Hkv, max_pages, num_pages, max_splits, chunk_pages;
+  int dense;             // 1: K/V are dense caches [B*Hkv, max_len, D], no block table
+  int max_len;           // longest valid context (dense: the cache rows; paged: table span)
   float scale_log2;
   int* status;
   unsigned long long timeout_ns;
@@ -122,7 +126,7 @@ __global__ void __launch_bounds__(160, 2)
   const int lane = tid & 31;
 
   int L = p.cu[b + 1] - p.cu[b];
-  if (L < 0 || L > p.max_pages * C::kPage) {
+  if (L < 0 || L > p.max_len) {
     if (split == 0 && tid == 0) report_status(p.status, -7);
     L = 0;
   }
@@ -168,13 +172,28 @@ __global__ void __launch_bounds__(160, 2)
     if (lane == 0) {
       prefetch_tensormap(&tm_k);
       prefetch_tensormap(&tm_v);
-      const int* row = p.table + static_cast<size_t>(b) * p.max_pages + pg0;
+      const int* row = p.dense ? nullptr : p.table + static_cast<size_t>(b) * p.max_pages + pg0;
       int issued = 0;
       for (int k = 0; k < n; ++k) {
         const int st = k % S;
         if (!mbar_wait(&ctl->empty[st], ((k / S) & 1) ^ 1, wc)) break;
-        const int phys = row[k];
         ++issued;
+        uint8_t* dst = ring + st * C::kStageBytes;
+        if (p.dense) {
+          // Page pg0 + k of the dense cache of (b, g): rows 64 (pg0 + k) .. + 63. Rows past
+          // the cache's end read as zeros; rows past L_b are masked by the consumers.
+          mbar_arrive_expect_tx(&ctl->full[st], C::kStageBytes);
+          const int plane = b * p.Hkv + g;
+#pragma unroll
+          for (int pn = 0; pn < C::kPanels; ++pn) {
+            tma_load_3d(dst + pn * C::kPanelBytes, &tm_k, &ctl->full[st], pn * 64,
+                        (pg0 + k) * C::kPage, plane);
+            tma_load_3d(dst + C::kPageBytes + pn * C::kPanelBytes, &tm_v, &ctl->full[st],
+                        pn * 64, (pg0 + k) * C::kPage, plane);
+          }
+          continue;
+        }
+        const int phys = row[k];
         if (phys < 0 || phys >= p.num_pages) {
           // Out-of-pool entry: never address it. The stage completes without data and the
           // status word tells the caller the result is invalid.
@@ -183,7 +202,6 @@ __global__ void __launch_bounds__(160, 2)
           continue;
         }
         mbar_arrive_expect_tx(&ctl->full[st], C::kStageBytes);
-        uint8_t* dst = ring + st * C::kStageBytes;
         const int plane = phys * p.Hkv + g;
 #pragma unroll
         for (int pn = 0; pn < C::kPanels; ++pn) {

@@ -25,6 +25,8 @@ MASK_CAUSAL = 1
 MASK_SLIDING = 2
 MASK_DOCUMENT = 3
 MASK_PAGED_DECODE = 4
+MASK_DECODE = 5
+DECODE_KINDS = (MASK_PAGED_DECODE, MASK_DECODE)
 
 PAGE_SIZE = 64
 # Poison written into unused page slots and spare pages: finite, and large enough that any
@@ -75,6 +77,7 @@ class Workload:
     DOCUMENT: B is the segment count and tensors are packed ``[1,H,T,d]`` with T = N.
     PAGED_DECODE: q, o ``[B,Hq,1,d]``; k, v pools ``[num_pages,Hkv,64,d]``;
     lse ``[B,Hq]``; N is the longest context.
+    DECODE: q, o ``[B,Hq,1,d]``; k, v dense caches ``[B,Hkv,N,d]``; lse ``[B,Hq]``.
     """
 
     name: str
@@ -95,7 +98,7 @@ class Workload:
 
     @property
     def out_shape(self):
-        if self.mask_kind == MASK_PAGED_DECODE:
+        if self.mask_kind in DECODE_KINDS:
             return (self.B, self.Hq, 1, self.d)
         if self.mask_kind == MASK_DOCUMENT:
             return (1, self.Hq, self.N, self.d)
@@ -103,7 +106,7 @@ class Workload:
 
     @property
     def lse_shape(self):
-        return self.out_shape[:-1] if self.mask_kind != MASK_PAGED_DECODE else (self.B, self.Hq)
+        return self.out_shape[:-1] if self.mask_kind not in DECODE_KINDS else (self.B, self.Hq)
 
     def valid_pairs_per_head(self) -> np.ndarray:
         """Number of visible (query, key) pairs for each batch entry / segment / sequence."""
@@ -120,14 +123,14 @@ class Workload:
         lens = np.diff(self.cu_seqlens.astype(np.int64))
         if self.mask_kind == MASK_DOCUMENT:
             return lens * (lens + 1) // 2
-        return lens  # paged decode: one query row sees all L_b keys
+        return lens  # decode: one query row sees all L_b keys
 
     def flops(self) -> float:
         """Algorithmic FLOPs 4 * Hq * d * (visible pairs), summed over batch/segments."""
         return 4.0 * self.Hq * self.d * float(self.valid_pairs_per_head().sum())
 
     def kv_bytes_valid(self) -> int:
-        """Paged decode: K+V bytes of the valid tokens (what an ideal kernel reads)."""
+        """Decode: K+V bytes of the valid tokens (what an ideal kernel reads)."""
         lens = np.diff(self.cu_seqlens.astype(np.int64))
         return int(lens.sum()) * self.Hkv * self.d * 2 * 2
 
@@ -217,6 +220,39 @@ def paged_decode_workload(seed: int, B: int, Lmin: int, Lmax: int, Hq: int, Hkv:
     return Workload(name or "paged_decode", MASK_PAGED_DECODE, B, Hq, Hkv, N, d,
                     default_scale(d), q, k_pool, v_pool, cu_seqlens=cu, block_table=table,
                     page_size=page_size)
+
+
+def dense_decode_workload(seed: int, B: int, Lmin: int, Lmax: int, Hq: int, Hkv: int, d: int,
+                          N: Optional[int] = None, context_lens: Optional[np.ndarray] = None,
+                          name: str = "") -> Workload:
+    """Decode problem on a dense per-sequence cache ``[B,Hkv,N,d]`` (N >= every length).
+
+    Draws lengths, q and the token-major K / V exactly as ``paged_decode_workload`` does with
+    the same arguments, so both describe the same attention problem; only the placement of
+    the keys differs. Slots past each sequence's end hold poison.
+    """
+    rng = np.random.default_rng(seed)
+    if context_lens is None:
+        lens = rng.integers(Lmin, Lmax + 1, size=B).astype(np.int64)
+    else:
+        lens = np.asarray(context_lens, dtype=np.int64)
+    q = normal_bf16(rng, (B, Hq, 1, d))
+    tot = int(lens.sum())
+    k_all = normal_bf16(rng, (Hkv, tot, d)) if tot else np.zeros((Hkv, 0, d), np.uint16)
+    v_all = normal_bf16(rng, (Hkv, tot, d)) if tot else np.zeros((Hkv, 0, d), np.uint16)
+    if N is None:
+        N = int(lens.max()) if B else 0
+    k = np.full((B, Hkv, N, d), f32_to_bf16_bits(np.float32(POISON_K)), dtype=np.uint16)
+    v = np.full((B, Hkv, N, d), f32_to_bf16_bits(np.float32(POISON_V)), dtype=np.uint16)
+    tok0 = 0
+    for b in range(B):
+        L = int(lens[b])
+        k[b, :, :L, :] = k_all[:, tok0: tok0 + L, :]
+        v[b, :, :L, :] = v_all[:, tok0: tok0 + L, :]
+        tok0 += L
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    return Workload(name or "dense_decode", MASK_DECODE, B, Hq, Hkv, N, d, default_scale(d),
+                    q, k, v, cu_seqlens=cu)
 
 
 # The five workloads the path is specified on, plus the causal shape the headline
