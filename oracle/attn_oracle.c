@@ -32,6 +32,14 @@
  *   DECODE     all j < L_b, key/value j of sequence b read from a dense per-sequence cache
  *              k[b, g, j, :] (the "standard attention kernel on the gathered layout" that
  *              is the second stage of Pattern C's two-stage path)
+ *   SLIDING_BIDIR  i - W <= j <= i + W (the "±W neighbors" of Pattern B taken literally:
+ *              W keys on each side of the query plus the query, clipped to [0, N))
+ *   DOCUMENT_BIDIR cu[s] <= j < cu[s+1] where cu[s] <= i < cu[s+1] (Pattern A's kernel as
+ *              printed: every key of the query's own segment, none outside it)
+ *   PREFIX_LM  j <= i or j < P, P = the prefix length passed as the window argument (the
+ *              prefix-LM mask the same page lists among masks with exploitable structure:
+ *              the first P tokens see each other in both directions, later tokens see
+ *              every earlier token)
  *
  * Inputs are raw bf16 bit patterns widened exactly to fp64. The fp32 scale is widened too.
  * A row that sees no key (impossible for valid inputs) gets O = 0 and LSE = -inf.
@@ -44,10 +52,14 @@
 #include <omp.h>
 #endif
 
-enum { OR_NONE = 0, OR_CAUSAL = 1, OR_SLIDING = 2, OR_DOCUMENT = 3, OR_PAGED = 4, OR_DECODE = 5 };
+enum { OR_NONE = 0, OR_CAUSAL = 1, OR_SLIDING = 2, OR_DOCUMENT = 3, OR_PAGED = 4, OR_DECODE = 5,
+       OR_SLIDING_BIDIR = 6, OR_DOCUMENT_BIDIR = 7, OR_PREFIX_LM = 8 };
 
 /* One query per sequence (PAGED, DECODE). */
 static int is_decode(int mask) { return mask == OR_PAGED || mask == OR_DECODE; }
+
+/* Packed segments described by cu_seqlens (DOCUMENT, DOCUMENT_BIDIR). */
+static int is_document(int mask) { return mask == OR_DOCUMENT || mask == OR_DOCUMENT_BIDIR; }
 
 typedef struct {
     const uint16_t *q, *k, *v;
@@ -69,7 +81,7 @@ static double widen_bf16(uint16_t bits) {
 /* Number of query rows, in the flattened order of the O / LSE outputs. */
 static int64_t row_count(const problem_t *P) {
     if (is_decode(P->mask)) return (int64_t)P->B * P->Hq;
-    if (P->mask == OR_DOCUMENT) return (int64_t)P->Hq * P->N;
+    if (is_document(P->mask)) return (int64_t)P->Hq * P->N;
     return (int64_t)P->B * P->Hq * P->N;
 }
 
@@ -79,7 +91,7 @@ static void row_coords(const problem_t *P, int64_t r, int *b, int *h, int *i) {
         *b = (int)(r / P->Hq);
         *h = (int)(r % P->Hq);
         *i = 0;
-    } else if (P->mask == OR_DOCUMENT) {
+    } else if (is_document(P->mask)) {
         *h = (int)(r / P->N);
         *i = (int)(r % P->N);
         int s = 0;
@@ -106,13 +118,16 @@ static int visible(const problem_t *P, int b, int i, int j) {
     case OR_DOCUMENT: return j <= i && j >= P->cu[b];
     case OR_PAGED:
     case OR_DECODE: return j < P->cu[b + 1] - P->cu[b];
+    case OR_SLIDING_BIDIR: return (int64_t)j >= (int64_t)i - P->W && (int64_t)j <= (int64_t)i + P->W;
+    case OR_DOCUMENT_BIDIR: return j >= P->cu[b] && j < P->cu[b + 1];
+    case OR_PREFIX_LM: return j <= i || j < P->W;
     }
     return 0;
 }
 
 static const uint16_t *query_row(const problem_t *P, int b, int h, int i) {
     if (is_decode(P->mask)) return P->q + ((size_t)b * P->Hq + h) * P->d;
-    if (P->mask == OR_DOCUMENT) return P->q + ((size_t)h * P->N + i) * P->d;
+    if (is_document(P->mask)) return P->q + ((size_t)h * P->N + i) * P->d;
     return P->q + (((size_t)b * P->Hq + h) * P->N + i) * P->d;
 }
 
@@ -122,7 +137,7 @@ static const uint16_t *kv_row(const problem_t *P, const uint16_t *base, int b, i
         int phys = P->table[(size_t)b * P->max_pages + j / P->page];
         return base + ((((size_t)phys * P->Hkv + g) * P->page) + (size_t)(j % P->page)) * P->d;
     }
-    if (P->mask == OR_DOCUMENT) return base + ((size_t)g * P->N + j) * P->d;
+    if (is_document(P->mask)) return base + ((size_t)g * P->N + j) * P->d;
     return base + (((size_t)b * P->Hkv + g) * P->N + j) * P->d;
 }
 
@@ -184,9 +199,10 @@ int oracle_attn(const uint16_t *q, const uint16_t *k, const uint16_t *v, int B, 
     problem_t P = {q, k, v, B, Hq, Hkv, N, d, (double)scale, mask_kind, window,
                    cu_seqlens, block_table, max_pages, page_size};
     if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || d <= 0 || N < 0) return -1;
-    if (mask_kind < OR_NONE || mask_kind > OR_DECODE) return -1;
+    if (mask_kind < OR_NONE || mask_kind > OR_PREFIX_LM) return -1;
     if (mask_kind == OR_SLIDING && window < 1) return -1;
-    if ((mask_kind == OR_DOCUMENT || is_decode(mask_kind)) && !cu_seqlens) return -1;
+    if ((mask_kind == OR_SLIDING_BIDIR || mask_kind == OR_PREFIX_LM) && window < 0) return -1;
+    if ((is_document(mask_kind) || is_decode(mask_kind)) && !cu_seqlens) return -1;
     for (int b = 0; mask_kind == OR_DECODE && b < B; b++) {
         const int L = cu_seqlens[b + 1] - cu_seqlens[b];
         if (L < 0 || L > N) return -1;  /* the dense cache holds N keys per sequence */

@@ -16,7 +16,8 @@ from tiled_attention_gb300 import inputs as I
 
 GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
 
-KINDS = ["none", "causal", "sliding", "document", "paged", "decode"]
+KINDS = ["none", "causal", "sliding", "document", "paged", "decode", "sliding_bidir",
+         "document_bidir", "prefix_lm"]
 
 
 def widen(bits):
@@ -28,7 +29,8 @@ def bf16(x):
 
 
 def tiny(kind: str, seed: int = 7, window: int = 5):
-    """Small problems with ragged sizes, GQA and several batch entries."""
+    """Small problems with ragged sizes, GQA and several batch entries. ``window`` is the
+    window of both sliding kinds and the prefix length of PREFIX_LM (default 9 there)."""
     if kind == "none":
         return I.dense_workload(seed, 2, 4, 2, 37, 16, I.MASK_NONE)
     if kind == "causal":
@@ -42,6 +44,14 @@ def tiny(kind: str, seed: int = 7, window: int = 5):
                                        context_lens=[1, 63, 130])
     if kind == "decode":
         return I.dense_decode_workload(seed, 3, 0, 0, 4, 2, 16, N=137, context_lens=[1, 63, 130])
+    if kind == "sliding_bidir":
+        return I.dense_workload(seed, 2, 4, 2, 37, 16, I.MASK_SLIDING_BIDIR, window=window)
+    if kind == "document_bidir":
+        return I.document_workload(seed, 37, 4, 16, cu_seqlens=[0, 5, 6, 20, 37], Hkv=2,
+                                   mask_kind=I.MASK_DOCUMENT_BIDIR)
+    if kind == "prefix_lm":
+        return I.dense_workload(seed, 2, 4, 2, 37, 16, I.MASK_PREFIX_LM,
+                                window=9 if window == 5 else window)
     raise KeyError(kind)
 
 
@@ -52,23 +62,32 @@ def dense_problems(w):
     with the mask written as whole-matrix torch operations (tril / triu / segment ids)."""
     qf, kf, vf = widen(w.q), widen(w.k), widen(w.v)
     group = w.Hq // w.Hkv
-    if w.mask_kind in (I.MASK_NONE, I.MASK_CAUSAL, I.MASK_SLIDING):
+    if w.mask_kind in (I.MASK_NONE, I.MASK_CAUSAL, I.MASK_SLIDING, I.MASK_SLIDING_BIDIR,
+                       I.MASK_PREFIX_LM):
         N = w.N
         ones = torch.ones(N, N, dtype=torch.bool)
         if w.mask_kind == I.MASK_NONE:
             mask = ones
         elif w.mask_kind == I.MASK_CAUSAL:
             mask = torch.tril(ones)
-        else:
+        elif w.mask_kind == I.MASK_SLIDING:
             mask = torch.tril(ones) & torch.triu(ones, diagonal=-(w.window - 1))
+        elif w.mask_kind == I.MASK_SLIDING_BIDIR:
+            mask = torch.tril(ones, diagonal=w.window) & torch.triu(ones, diagonal=-w.window)
+        else:  # prefix-LM: the lower triangle plus the first P columns
+            prefix = torch.zeros(N, N, dtype=torch.bool)
+            prefix[:, :w.window] = True
+            mask = torch.tril(ones) | prefix
         for b in range(w.B):
             for h in range(w.Hq):
                 rows = (b * w.Hq + h) * N + np.arange(N)
                 yield rows, qf[b, h], kf[b, h // group], vf[b, h // group], mask.numpy()
-    elif w.mask_kind == I.MASK_DOCUMENT:
+    elif w.mask_kind in I.DOCUMENT_KINDS:
         T = w.N
         seg = torch.bucketize(torch.arange(T), torch.as_tensor(w.cu_seqlens[1:]), right=True)
-        mask = (seg[:, None] == seg[None, :]) & torch.tril(torch.ones(T, T, dtype=torch.bool))
+        mask = seg[:, None] == seg[None, :]
+        if w.mask_kind == I.MASK_DOCUMENT:
+            mask = mask & torch.tril(torch.ones(T, T, dtype=torch.bool))
         for h in range(w.Hq):
             rows = h * T + np.arange(T)
             yield rows, qf[0, h], kf[0, h // group], vf[0, h // group], mask.numpy()
@@ -170,7 +189,7 @@ def _set_dominant(w, r, jstar):
         w.k[b, g, :, 0] = 0
         w.k[b, g, jstar, 0] = bf16(32.0)
         return
-    if w.mask_kind == I.MASK_DOCUMENT:
+    if w.mask_kind in I.DOCUMENT_KINDS:
         h, i = divmod(r, w.N)
         b = 0
     else:
@@ -199,6 +218,10 @@ def pin_probabilities(attn, kind):
 def pin_single_key_rows(attn, kind):
     """A row that sees exactly one key returns that key's V row exactly and LSE = its score."""
     if kind == "sliding":
+        w = tiny(kind, window=1)
+    elif kind == "sliding_bidir":
+        w = tiny(kind, window=0)
+    elif kind == "prefix_lm":
         w = tiny(kind, window=1)
     elif kind == "none":
         w = I.dense_workload(5, 2, 4, 2, 1, 16, I.MASK_NONE)
@@ -287,8 +310,9 @@ def pin_gqa_equals_repeated_mha(attn, kind):
         m.block_table = w.block_table.copy()
     elif kind == "decode":
         m = I.dense_decode_workload(7, 3, 0, 0, 4, 4, 16, N=137, context_lens=[1, 63, 130])
-    elif kind == "document":
-        m = I.document_workload(7, 37, 4, 16, cu_seqlens=[0, 5, 6, 20, 37], Hkv=4)
+    elif kind in ("document", "document_bidir"):
+        m = I.document_workload(7, 37, 4, 16, cu_seqlens=[0, 5, 6, 20, 37], Hkv=4,
+                                mask_kind=w.mask_kind)
     else:
         m = I.dense_workload(7, 2, 4, 4, 37, 16, w.mask_kind, window=w.window)
     m.q[...] = w.q
@@ -296,6 +320,79 @@ def pin_gqa_equals_repeated_mha(attn, kind):
     m.v[...] = np.repeat(w.v, group, axis=1)
     assert np.array_equal(attn(m)[0], attn(w)[0])
     assert np.array_equal(attn(m)[1], attn(w)[1])
+
+
+def pin_bidir_window_limits(attn):
+    """A two-sided window that covers every key is no mask at all; one that covers none but
+    the query (W = 0) returns each row's own V row; and the two-sided window W is the union
+    of the causal window W + 1 and its mirror image (checked on the probabilities: the row
+    of query i is non-zero exactly at keys i - W .. i + W)."""
+    n = tiny("none")
+    for W in (n.N - 1, n.N, 10 * n.N):
+        s = tiny("sliding_bidir", window=W)
+        assert np.array_equal(attn(s)[0], attn(n)[0])
+        assert np.array_equal(attn(s)[1], attn(n)[1])
+    s = tiny("sliding_bidir", window=n.N - 2)
+    assert not np.array_equal(attn(s)[0], attn(n)[0])
+    w0 = tiny("sliding_bidir", window=0)
+    o, _ = attn(w0)
+    vv = widen(w0.v)
+    group = w0.Hq // w0.Hkv
+    for b in range(w0.B):
+        for h in range(w0.Hq):
+            rows = (b * w0.Hq + h) * w0.N + np.arange(w0.N)
+            assert np.array_equal(o[rows], vv[b, h // group])
+    w = tiny("sliding_bidir", window=3)
+    _, _, p = attn(w, probs=True)
+    for r in range(p.shape[0]):
+        i = r % w.N
+        nz = np.nonzero(p[r])[0]
+        assert list(nz) == list(range(max(0, i - 3), min(w.N, i + 4)))
+
+
+def pin_prefix_limits(attn):
+    """A prefix of 0 or 1 tokens is the causal mask; a prefix covering the sequence is no
+    mask; with Q = 0 every visible score is 0, so row i's LSE is the log of its visible key
+    count, max(i + 1, P)."""
+    c = tiny("causal")
+    n = tiny("none")
+    for P in (0, 1):
+        s = tiny("prefix_lm", window=P)
+        assert np.array_equal(attn(s)[0], attn(c)[0])
+        assert np.array_equal(attn(s)[1], attn(c)[1])
+    for P in (n.N, n.N + 5):
+        s = tiny("prefix_lm", window=P)
+        assert np.array_equal(attn(s)[0], attn(n)[0])
+        assert np.array_equal(attn(s)[1], attn(n)[1])
+    w = tiny("prefix_lm", window=9)
+    w.q[...] = 0
+    o, lse = attn(w)
+    for r in range(o.shape[0]):
+        i = r % w.N
+        assert abs(lse[r] - math.log(max(i + 1, 9))) < 1e-13
+
+
+def pin_document_bidir_segments(attn):
+    """Non-causal document attention equals unmasked attention run on each segment alone,
+    and a single segment is no mask at all."""
+    w = tiny("document_bidir")
+    o, lse = attn(w)
+    cu = w.cu_seqlens
+    for s in range(len(cu) - 1):
+        a, e = int(cu[s]), int(cu[s + 1])
+        L = e - a
+        d = I.dense_workload(0, 1, w.Hq, w.Hkv, L, w.d, I.MASK_NONE)
+        d.q[0], d.k[0], d.v[0] = w.q[0, :, a:e], w.k[0, :, a:e], w.v[0, :, a:e]
+        od, ld = attn(d)
+        rows = (np.arange(w.Hq)[:, None] * w.N + np.arange(a, e)[None, :]).reshape(-1)
+        assert np.array_equal(od, o[rows])
+        assert np.array_equal(ld, lse[rows])
+    n = I.dense_workload(11, 1, 4, 2, 37, 16, I.MASK_NONE)
+    d = I.document_workload(11, 37, 4, 16, cu_seqlens=[0, 37], Hkv=2,
+                            mask_kind=I.MASK_DOCUMENT_BIDIR)
+    d.q[...], d.k[...], d.v[...] = n.q, n.k, n.v
+    assert np.array_equal(attn(d)[0], attn(n)[0])
+    assert np.array_equal(attn(d)[1], attn(n)[1])
 
 
 def pin_paged_equals_dense_last_row(attn):
@@ -385,6 +482,7 @@ def all_pins():
             pins.append((f"{f.__name__}[{kind}]", (lambda f, kind: lambda a: f(a, kind))(f, kind)))
     for f in (pin_key_permutation, pin_window_covering_equals_causal,
               pin_single_segment_equals_causal, pin_paged_equals_dense_last_row,
-              pin_dense_decode_equals_paged, pin_closed_form_golden):
+              pin_dense_decode_equals_paged, pin_bidir_window_limits, pin_prefix_limits,
+              pin_document_bidir_segments, pin_closed_form_golden):
         pins.append((f.__name__, f))
     return pins

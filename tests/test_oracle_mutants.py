@@ -29,6 +29,19 @@ MUTANTS = [
      "if (visible(P, b, i, j)) l += exp(z[j]);"),
     ("lse_sign", "*lse = M + log(l);", "*lse = M - log(l);"),
     ("no_normalise", "for (int c = 0; c < P->d; c++) o[c] /= l;", ""),
+    ("bidir_window_one_sided",
+     "return (int64_t)j >= (int64_t)i - P->W && (int64_t)j <= (int64_t)i + P->W;",
+     "return (int64_t)j >= (int64_t)i - P->W && (int64_t)j <= (int64_t)i;"),
+    ("bidir_window_narrow",
+     "return (int64_t)j >= (int64_t)i - P->W && (int64_t)j <= (int64_t)i + P->W;",
+     "return (int64_t)j > (int64_t)i - P->W && (int64_t)j < (int64_t)i + P->W;"),
+    ("document_bidir_end_inclusive",
+     "case OR_DOCUMENT_BIDIR: return j >= P->cu[b] && j < P->cu[b + 1];",
+     "case OR_DOCUMENT_BIDIR: return j >= P->cu[b] && j <= P->cu[b + 1];"),
+    ("prefix_off_by_one", "case OR_PREFIX_LM: return j <= i || j < P->W;",
+     "case OR_PREFIX_LM: return j <= i || j <= P->W;"),
+    ("prefix_ignored", "case OR_PREFIX_LM: return j <= i || j < P->W;",
+     "case OR_PREFIX_LM: return j <= i;"),
     ("query_transposed", "return P->q + (((size_t)b * P->Hq + h) * P->N + i) * P->d;",
      "return P->q + (((size_t)b * P->Hq + h) * P->N) * P->d + i;"),
 ]

@@ -45,7 +45,12 @@ def test_thread_count_does_not_change_results():
 def test_workload_pair_counts():
     """The pair counts used for FLOP accounting, checked by direct enumeration."""
     for kind, w in [("causal", tiny("causal")), ("sliding", tiny("sliding")),
-                    ("document", tiny("document")), ("none", tiny("none"))]:
+                    ("document", tiny("document")), ("none", tiny("none")),
+                    ("sliding_bidir", tiny("sliding_bidir")),
+                    ("sliding_bidir", tiny("sliding_bidir", window=40)),
+                    ("document_bidir", tiny("document_bidir")),
+                    ("prefix_lm", tiny("prefix_lm")),
+                    ("prefix_lm", tiny("prefix_lm", window=50))]:
         _, _, p = oracle.attention(w, probs=True)
         per_head = (p > 0).sum() / w.Hq
         if kind == "document":

@@ -26,7 +26,11 @@ MASK_SLIDING = 2
 MASK_DOCUMENT = 3
 MASK_PAGED_DECODE = 4
 MASK_DECODE = 5
+MASK_SLIDING_BIDIR = 6
+MASK_DOCUMENT_BIDIR = 7
+MASK_PREFIX_LM = 8
 DECODE_KINDS = (MASK_PAGED_DECODE, MASK_DECODE)
+DOCUMENT_KINDS = (MASK_DOCUMENT, MASK_DOCUMENT_BIDIR)
 
 PAGE_SIZE = 64
 # Poison written into unused page slots and spare pages: finite, and large enough that any
@@ -74,7 +78,9 @@ class Workload:
     """One attention forward problem in the layouts of the C ABI.
 
     Dense kinds: q, o ``[B,Hq,N,d]``; k, v ``[B,Hkv,N,d]``; lse ``[B,Hq,N]``.
-    DOCUMENT: B is the segment count and tensors are packed ``[1,H,T,d]`` with T = N.
+    DOCUMENT, DOCUMENT_BIDIR: B is the segment count and tensors are packed ``[1,H,T,d]``
+    with T = N.
+    SLIDING and SLIDING_BIDIR take the window, PREFIX_LM the prefix length, in ``window``.
     PAGED_DECODE: q, o ``[B,Hq,1,d]``; k, v pools ``[num_pages,Hkv,64,d]``;
     lse ``[B,Hq]``; N is the longest context.
     DECODE: q, o ``[B,Hq,1,d]``; k, v dense caches ``[B,Hkv,N,d]``; lse ``[B,Hq]``.
@@ -100,7 +106,7 @@ class Workload:
     def out_shape(self):
         if self.mask_kind in DECODE_KINDS:
             return (self.B, self.Hq, 1, self.d)
-        if self.mask_kind == MASK_DOCUMENT:
+        if self.mask_kind in DOCUMENT_KINDS:
             return (1, self.Hq, self.N, self.d)
         return (self.B, self.Hq, self.N, self.d)
 
@@ -120,9 +126,19 @@ class Workload:
             # rows i < w see i+1 keys, rows i >= w see w keys
             cnt = full * (full + 1) // 2 + max(0, n - w) * w
             return np.full(self.B, cnt, dtype=np.int64)
+        if self.mask_kind == MASK_SLIDING_BIDIR:
+            i = np.arange(self.N, dtype=np.int64)
+            cnt = (np.minimum(i + self.window, self.N - 1) - np.maximum(i - self.window, 0) + 1)
+            return np.full(self.B, int(cnt.sum()), dtype=np.int64)
+        if self.mask_kind == MASK_PREFIX_LM:
+            i = np.arange(self.N, dtype=np.int64)
+            cnt = np.minimum(np.maximum(i + 1, self.window), self.N)
+            return np.full(self.B, int(cnt.sum()), dtype=np.int64)
         lens = np.diff(self.cu_seqlens.astype(np.int64))
         if self.mask_kind == MASK_DOCUMENT:
             return lens * (lens + 1) // 2
+        if self.mask_kind == MASK_DOCUMENT_BIDIR:
+            return lens * lens
         return lens  # decode: one query row sees all L_b keys
 
     def flops(self) -> float:
@@ -160,14 +176,14 @@ def draw_segments(rng: np.random.Generator, total: int, lo: int, hi: int) -> np.
 
 def document_workload(seed: int, T: int, H: int, d: int, lo: int = 256, hi: int = 4096,
                       cu_seqlens: Optional[np.ndarray] = None, Hkv: Optional[int] = None,
-                      name: str = "") -> Workload:
+                      name: str = "", mask_kind: int = MASK_DOCUMENT) -> Workload:
     rng = np.random.default_rng(seed)
     cu = draw_segments(rng, T, lo, hi) if cu_seqlens is None else np.asarray(cu_seqlens, np.int32)
     hkv = H if Hkv is None else Hkv
     q = normal_bf16(rng, (1, H, T, d))
     k = normal_bf16(rng, (1, hkv, T, d))
     v = normal_bf16(rng, (1, hkv, T, d))
-    return Workload(name or "document", MASK_DOCUMENT, len(cu) - 1, H, hkv, T, d,
+    return Workload(name or "document", mask_kind, len(cu) - 1, H, hkv, T, d,
                     default_scale(d), q, k, v, cu_seqlens=cu)
 
 
