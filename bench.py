@@ -11,6 +11,7 @@ One step = one pass of the whole path over one batch of synthetic input:
 decode) are larger than L2, so no flush is needed between steps.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+       python bench.py --suite [--steps K]   (every workload, one JSON line each)
 For N > 1 it runs under torch.distributed.run, one rank per GPU, each rank an independent
 replica of the step (the path has no exchange step); value sums all ranks' work over the
 slowest rank's time.
@@ -205,6 +206,106 @@ def reference_arm(args, rank: int):
     print(json.dumps(line), flush=True)
 
 
+def suite(args):
+    """Time every specified workload and the mask variants one launch at a time (median of
+    --steps launches after --warmup, L2 flushed before each launch by writing a 256 MB
+    buffer), plus the two-stage paged decode (page gather, then decode on the dense copy)
+    next to the fused paged decode. Prints one JSON line per workload."""
+    import torch
+    from tiled_attention_gb300 import attn, build
+    from tiled_attention_gb300 import inputs as I
+    from tiled_attention_gb300.runner import DeviceProblem
+    build.build()
+    attn.lib()
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream(dev)
+    peaks = load_peaks()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    tag = "of " + peaks["source"]
+
+    def timed(fn, reps):
+        times = []
+        for k in range(args.warmup + reps):
+            flush.fill_(k & 0xFF)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            rc = fn()
+            e1.record(stream)
+            assert rc == 0, attn.last_error()
+            if k >= args.warmup:
+                times.append((e0, e1))
+        torch.cuda.synchronize(dev)
+        assert attn.attn_get_status(stream) == 0
+        return float(np.median([a.elapsed_time(b) for a, b in times]))
+
+    def dec_bytes(w):
+        return (w.kv_bytes_valid() + w.q.nbytes * 2 + w.B * w.Hq * 4 +
+                (w.block_table.nbytes if w.block_table is not None else 0) +
+                w.cu_seqlens.nbytes)
+
+    def emit(w, ms, extra=None):
+        line = {"suite": True, "workload": w.name, "mask_kind": w.mask_kind, "d": w.d,
+                "ms": ms, "launches_timed": args.steps}
+        if w.mask_kind in I.DECODE_KINDS:
+            gbs = dec_bytes(w) / (ms * 1e-3) / 1e9
+            line.update(value=gbs, unit="GB/s", frac=gbs / peaks["hbm_gbs"],
+                        peak=f"HBM copy {tag}")
+        else:
+            tf = w.flops() / (ms * 1e-3) / 1e12
+            line.update(value=tf, unit="TFLOP/s", frac=tf / peaks["bf16_tflops"],
+                        peak=f"bf16 burst {tag}", flops=w.flops())
+        if extra:
+            line.update(extra)
+        print(json.dumps(line), flush=True)
+
+    for cfg in (1, 2, 3, "3c", 4, "3b", "3p", "4b", 5):
+        w = I.config(cfg)
+        dp = DeviceProblem(w, device=dev, fill_outputs=0.0)
+        emit(w, timed(lambda: dp.run(stream), args.steps))
+        if cfg == 5:
+            # Two-stage path of the paged-KV pattern: gather K and V pages into dense caches,
+            # then the decode kernel reads the caches.
+            max_pages = w.block_table.shape[1]
+            L = max_pages * w.page_size
+            kd = torch.empty((w.B, w.Hkv, L, w.d), dtype=torch.bfloat16, device=dev)
+            vd = torch.empty_like(kd)
+            o = torch.empty_like(dp.o)
+            lse = torch.empty_like(dp.lse)
+            nb = attn.attn_workspace_bytes(w.B, w.Hq, w.Hkv, L, w.d, attn.ATTN_MASK_DECODE, 0)
+            ws = torch.empty(nb, dtype=torch.uint8, device=dev)
+            pages = int(((np.diff(w.cu_seqlens) + w.page_size - 1) // w.page_size).sum())
+            page_bytes = w.Hkv * w.page_size * w.d * 2
+
+            def gather():
+                rc = attn.attn_gather_pages(dp.k, kd, dp.table, w.B, max_pages, w.Hkv,
+                                            w.page_size, w.d, dp.num_pages, stream)
+                return rc | attn.attn_gather_pages(dp.v, vd, dp.table, w.B, max_pages, w.Hkv,
+                                                   w.page_size, w.d, dp.num_pages, stream)
+
+            def dense():
+                return attn.attn_fwd(dp.q, kd, vd, o, lse, w.B, w.Hq, w.Hkv, L, w.d, w.scale,
+                                     attn.ATTN_MASK_DECODE, 0, dp.cu, None, 0, 0, ws, stream)
+
+            g_ms = timed(gather, args.steps)
+            d_ms = timed(dense, args.steps)
+            both_ms = timed(lambda: gather() | dense(), args.steps)
+            g_bytes = 2 * 2 * pages * page_bytes  # K and V pages, read once and written once
+            print(json.dumps({
+                "suite": True, "workload": "two-stage paged decode (gather + dense decode) "
+                "on " + w.name, "ms": both_ms, "launches_timed": args.steps,
+                "gather_ms": g_ms, "gather_gbs": g_bytes / (g_ms * 1e-3) / 1e9,
+                "gather_bytes": g_bytes, "dense_decode_ms": d_ms,
+                "dense_decode_gbs": dec_bytes(w) / (d_ms * 1e-3) / 1e9,
+                "bytes_moved": g_bytes + dec_bytes(w), "fused_bytes": dec_bytes(w),
+                "unit": "GB/s (valid K+V per decode)",
+                "value": dec_bytes(w) / (both_ms * 1e-3) / 1e9}), flush=True)
+            del kd, vd, ws
+        del dp
+        torch.cuda.empty_cache()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -216,8 +317,13 @@ def main():
                     help="seconds of oracle work for the CPU baseline (rank 0, N=1 only)")
     ap.add_argument("--only", choices=["prefill", "decode"], default=None,
                     help="time one part of the step only (for profiler captures)")
+    ap.add_argument("--suite", action="store_true",
+                    help="time every workload one launch at a time (one JSON line each)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
+    if args.suite:
+        suite(args)
+        return
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

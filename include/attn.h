@@ -40,16 +40,26 @@ extern "C" {
  *  PAGED_DECODE  one query per sequence sees its whole context, read through a block table
  *                (same page, Pattern C).
  *  DECODE        one query per sequence sees its whole context, read from a dense
- *                per-sequence cache: the second stage ("standard attention kernel on the
- *                gathered layout") of the two-stage paged path of the same page, Pattern C,
- *                whose first stage is attn_gather_pages. */
+ *                per-sequence cache: the second stage of the two-stage paged path of the
+ *                same page, Pattern C (an ordinary attention kernel run on pages that
+ *                attn_gather_pages has gathered).
+ *  SLIDING_BIDIR i - window <= j <= i + window: Pattern B's neighbourhood of W keys on
+ *                both sides taken literally (window >= 0 keys on each side of the query).
+ *  DOCUMENT_BIDIR cu_seqlens[s] <= j < cu_seqlens[s+1] where segment s holds i: Pattern A's
+ *                kernel as printed (every key of the query's own segment, none outside it).
+ *  PREFIX_LM     j <= i or j < window: a prefix of `window` tokens that see each other in
+ *                both directions, then causal rows (the prefix-LM mask the same page lists
+ *                among masks whose structure a kernel should exploit). */
 enum attn_mask_kind {
     ATTN_MASK_NONE = 0,
     ATTN_MASK_CAUSAL = 1,
     ATTN_MASK_SLIDING = 2,
     ATTN_MASK_DOCUMENT = 3,
     ATTN_MASK_PAGED_DECODE = 4,
-    ATTN_MASK_DECODE = 5
+    ATTN_MASK_DECODE = 5,
+    ATTN_MASK_SLIDING_BIDIR = 6,
+    ATTN_MASK_DOCUMENT_BIDIR = 7,
+    ATTN_MASK_PREFIX_LM = 8
 };
 
 enum attn_status {
@@ -66,24 +76,29 @@ enum attn_status {
 /*
  * attn_fwd — fused tiled attention forward pass.
  *
- * q, o      bf16. Dense kinds [B,Hq,N,d]; DOCUMENT [1,Hq,N,d] with N = total packed tokens;
- *           PAGED_DECODE and DECODE [B,Hq,1,d].
- * k, v      bf16. Dense kinds [B,Hkv,N,d]; DOCUMENT [1,Hkv,N,d]; PAGED_DECODE page pools
+ * The document kinds are DOCUMENT and DOCUMENT_BIDIR; the dense kinds are NONE, CAUSAL,
+ * SLIDING, SLIDING_BIDIR and PREFIX_LM.
+ * q, o      bf16. Dense kinds [B,Hq,N,d]; document kinds [1,Hq,N,d] with N = total packed
+ *           tokens; PAGED_DECODE and DECODE [B,Hq,1,d].
+ * k, v      bf16. Dense kinds [B,Hkv,N,d]; document kinds [1,Hkv,N,d]; PAGED_DECODE page pools
  *           [num_pages,Hkv,page_size,d] (one (page, kv-head) block is contiguous); DECODE
  *           dense caches [B,Hkv,N,d] (rows past a sequence's length are never read into the
  *           result).
- * lse       fp32, ln sum_j exp(scale * q_i . k_j) over the visible keys. [B,Hq,N]; DOCUMENT
- *           [1,Hq,N]; PAGED_DECODE and DECODE [B,Hq].
- * B         batch (dense), number of segments (DOCUMENT) or sequences (PAGED_DECODE).
+ * lse       fp32, ln sum_j exp(scale * q_i . k_j) over the visible keys. [B,Hq,N]; document
+ *           kinds [1,Hq,N]; PAGED_DECODE and DECODE [B,Hq].
+ * B         batch (dense), number of segments (document kinds) or sequences (decode kinds).
  * Hq, Hkv   query / key-value heads; Hq % Hkv == 0; query head h reads kv head h/(Hq/Hkv).
- * N         keys per sequence (dense), packed tokens (DOCUMENT), the longest context
+ * N         keys per sequence (dense), packed tokens (document kinds), the longest context
  *           (PAGED_DECODE: block_table has ceil(N/page_size) columns), or the rows of each
  *           dense cache (DECODE).
  * d         head dimension; 64 or 128 (else ATTN_ERR_UNSUPPORTED).
  * scale     multiplies q.k before the softmax (callers usually pass 1/sqrt(d)).
  * mask_kind enum attn_mask_kind.
- * window    SLIDING only: number of keys visible to a query (>= 1). Ignored otherwise.
- * cu_seqlens int32 device array [B+1], cu[0] = 0, nondecreasing. DOCUMENT: segment starts,
+ * window    SLIDING: number of keys visible to a query (>= 1). SLIDING_BIDIR: keys visible
+ *           on each side of the query (>= 0). PREFIX_LM: prefix length (>= 0; 0 and 1 give
+ *           the causal mask, >= N no mask). Ignored otherwise. Out of range:
+ *           ATTN_ERR_INVALID.
+ * cu_seqlens int32 device array [B+1], cu[0] = 0, nondecreasing. Document kinds: segment starts,
  *           cu[B] = N. PAGED_DECODE and DECODE: cumulative context lengths
  *           (L_b = cu[b+1] - cu[b], 0 <= L_b <= N). Checked on the device (status
  *           ATTN_ERR_SEQLENS). Unused otherwise.
@@ -170,7 +185,7 @@ int attn_version(void);
  * attn_plan_kv_range: for query rows [r0, min(r0+bm, row_end)) and keys indexed from k_org
  * (valid keys [k_org, k_end)), the half-open range [*lo, *hi) of bn-wide key tiles (tile t
  * covers keys k_org + t*bn ... + bn-1) holding at least one visible pair. *hi <= *lo when
- * none does. Returns 0, or ATTN_ERR_INVALID.
+ * none does. Returns 0, or ATTN_ERR_INVALID (a decode kind, or a window out of range).
  *
  * attn_plan_tile_kind: 0 if tile t holds no visible pair for those rows, 1 if every (row,
  * key) pair in it is visible (no element mask needed), 2 if it is a boundary tile.
@@ -184,7 +199,8 @@ int attn_plan_tile_kind(int mask_kind, int window, int r0, int bm, int row_end, 
  * attn_plan_units: the prefill work list in launch order. One unit is a pair of bm-row query
  * tiles of one (batch or segment, query head); units are ordered longest-first (pair index
  * descending), then by batch/segment, then head, so the heaviest causal tiles start first and
- * heads sharing a kv head run side by side. cu_seqlens is a HOST array here (DOCUMENT only).
+ * heads sharing a kv head run side by side. cu_seqlens is a HOST array here (document kinds
+ * only).
  * Writes up to max_units records of 3 ints (segment or batch, head, pair index) to out and
  * returns the unit count (or a negative ATTN_ERR_*).
  */

@@ -22,7 +22,7 @@
  * Visible sets (readings of the pages fixed for this build):
  *   NONE       all j < N
  *   CAUSAL     j <= i
- *   SLIDING    i - W < j <= i   (causal, W keys including the query itself; the "±W"
+ *   SLIDING    i - W < j <= i   (causal, W keys including the query itself; the two-sided
  *              wording of "Optimizing Triton Kernels for Custom Attention Patterns on H100",
  *              Pattern B, is read as this causal window)
  *   DOCUMENT   cu[s] <= j <= i where cu[s] <= i < cu[s+1] (causal inside the query's own
@@ -30,9 +30,9 @@
  *   PAGED      all j < L_b, key/value j of sequence b read from physical page
  *              table[b][j / page] at slot j % page (the block-table indirection of Pattern C)
  *   DECODE     all j < L_b, key/value j of sequence b read from a dense per-sequence cache
- *              k[b, g, j, :] (the "standard attention kernel on the gathered layout" that
- *              is the second stage of Pattern C's two-stage path)
- *   SLIDING_BIDIR  i - W <= j <= i + W (the "±W neighbors" of Pattern B taken literally:
+ *              k[b, g, j, :] (the plain attention kernel run on the gathered pages, the
+ *              second stage of Pattern C's two-stage path)
+ *   SLIDING_BIDIR  i - W <= j <= i + W (Pattern B's plus-or-minus-W neighbourhood taken literally:
  *              W keys on each side of the query plus the query, clipped to [0, N))
  *   DOCUMENT_BIDIR cu[s] <= j < cu[s+1] where cu[s] <= i < cu[s+1] (Pattern A's kernel as
  *              printed: every key of the query's own segment, none outside it)

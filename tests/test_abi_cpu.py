@@ -9,6 +9,7 @@ import pytest
 from tiled_attention_gb300 import attn, build
 
 NONE, CAUSAL, SLIDING, DOCUMENT = 0, 1, 2, 3
+SLIDING_BIDIR, DOCUMENT_BIDIR, PREFIX_LM = 6, 7, 8
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -39,7 +40,11 @@ def _call(**kw):
 
 
 @pytest.mark.parametrize("kw,code", [
-    (dict(mask_kind=7), attn.ATTN_ERR_INVALID),
+    (dict(mask_kind=9), attn.ATTN_ERR_INVALID),
+    (dict(mask_kind=-1), attn.ATTN_ERR_INVALID),
+    (dict(mask_kind=SLIDING_BIDIR, window=-1), attn.ATTN_ERR_INVALID),
+    (dict(mask_kind=PREFIX_LM, window=-3), attn.ATTN_ERR_INVALID),
+    (dict(mask_kind=DOCUMENT_BIDIR), attn.ATTN_ERR_INVALID),  # no cu_seqlens
     (dict(Hq=6, Hkv=4), attn.ATTN_ERR_INVALID),
     (dict(d=96), attn.ATTN_ERR_UNSUPPORTED),
     (dict(d=256), attn.ATTN_ERR_UNSUPPORTED),
@@ -104,10 +109,14 @@ def visible(mask, W, k_org, k_end, i, j):
     """Key j visible to query row i (keys and rows share one index space)."""
     if j < k_org or j >= k_end:
         return False
-    if mask == NONE:
+    if mask in (NONE, DOCUMENT_BIDIR):
         return True
     if mask == CAUSAL or mask == DOCUMENT:
         return j <= i
+    if mask == SLIDING_BIDIR:
+        return i - W <= j <= i + W
+    if mask == PREFIX_LM:
+        return j <= i or j < W
     return i - W < j <= i
 
 
@@ -142,6 +151,10 @@ def test_schedule_dense_exhaustive(bm, bn):
             check_schedule(CAUSAL, 0, r0, bm, N, 0, N, bn)
             for W in (1, 2, 3, 4, 5, 7, 8, 9, N, N + 3):
                 check_schedule(SLIDING, W, r0, bm, N, 0, N, bn)
+            for W in (0, 1, 2, 3, 4, 5, 8, 9, N, N + 3, 2**31 - 1):
+                check_schedule(SLIDING_BIDIR, W, r0, bm, N, 0, N, bn)
+            for P in (0, 1, 2, 3, 4, 5, 8, 9, N - 1, N, N + 3):
+                check_schedule(PREFIX_LM, max(P, 0), r0, bm, N, 0, N, bn)
 
 
 @pytest.mark.parametrize("bm,bn", [(4, 4), (4, 8), (8, 4)])
@@ -150,6 +163,7 @@ def test_schedule_document_exhaustive(bm, bn):
     for s in range(len(cu) - 1):
         for r0 in range(cu[s], cu[s + 1], bm):
             check_schedule(DOCUMENT, 0, r0, bm, cu[s + 1], cu[s], cu[s + 1], bn)
+            check_schedule(DOCUMENT_BIDIR, 0, r0, bm, cu[s + 1], cu[s], cu[s + 1], bn)
 
 
 def test_schedule_kernel_tile_sizes():
@@ -160,6 +174,36 @@ def test_schedule_kernel_tile_sizes():
             check_schedule(NONE, 0, r0, 128, N, 0, N, 128)
             for W in (1, 127, 128, 129, 200):
                 check_schedule(SLIDING, W, r0, 128, N, 0, N, 128)
+                check_schedule(SLIDING_BIDIR, W, r0, 128, N, 0, N, 128)
+                check_schedule(PREFIX_LM, W, r0, 128, N, 0, N, 128)
+
+
+def test_plan_rejects_decode_kinds_and_bad_windows():
+    for kind in (attn.ATTN_MASK_PAGED_DECODE, attn.ATTN_MASK_DECODE, 9):
+        with pytest.raises(attn.AttnError):
+            attn.attn_plan_kv_range(kind, 1, 0, 128, 256, 0, 256, 128)
+        assert attn.attn_plan_tile_kind(kind, 1, 0, 128, 256, 0, 256, 128, 0) < 0
+    with pytest.raises(attn.AttnError):
+        attn.attn_plan_kv_range(SLIDING_BIDIR, -1, 0, 128, 256, 0, 256, 128)
+
+
+def test_schedule_bidir_and_prefix_shapes():
+    """Two-sided window 2048 at N=8192 with 128-wide tiles: 33 key tiles away from the ends,
+    two of them boundary tiles; prefix 4096: the first 16 query tiles read the 32 prefix
+    tiles, all full except the diagonal ones past the prefix."""
+    for r in range(64):
+        lo, hi = attn.attn_plan_kv_range(SLIDING_BIDIR, 2048, 128 * r, 128, 8192, 0, 8192, 128)
+        kinds = [attn.attn_plan_tile_kind(SLIDING_BIDIR, 2048, 128 * r, 128, 8192, 0, 8192,
+                                          128, t) for t in range(lo, hi)]
+        if 16 <= r < 48:
+            assert (lo, hi) == (r - 16, r + 17)
+        assert kinds.count(2) <= 2 and 0 not in kinds
+    for r in range(64):
+        lo, hi = attn.attn_plan_kv_range(PREFIX_LM, 4096, 128 * r, 128, 8192, 0, 8192, 128)
+        assert (lo, hi) == (0, max(32, r + 1))
+        kinds = [attn.attn_plan_tile_kind(PREFIX_LM, 4096, 128 * r, 128, 8192, 0, 8192, 128, t)
+                 for t in range(lo, hi)]
+        assert kinds == ([1] * 32 if r < 32 else [1] * r + [2])
 
 
 def test_schedule_skips_masked_tiles():
@@ -181,9 +225,10 @@ def test_schedule_skips_masked_tiles():
         assert hi - lo <= 33 and kinds.count(2) <= 2 and 0 not in kinds
 
 
-def test_units_dense_order_and_cover():
+@pytest.mark.parametrize("kind", [NONE, CAUSAL, SLIDING_BIDIR, PREFIX_LM])
+def test_units_dense_order_and_cover(kind):
     B, Hq, N = 2, 3, 700
-    u = attn.attn_plan_units(CAUSAL, B, Hq, N)
+    u = attn.attn_plan_units(kind, B, Hq, N)
     npairs = (N + 255) // 256
     assert len(u) == B * Hq * npairs
     assert sorted(u) == sorted(itertools.product(range(B), range(Hq), range(npairs)))
@@ -191,10 +236,11 @@ def test_units_dense_order_and_cover():
     assert levels == sorted(levels, reverse=True)
 
 
-def test_units_document_order_and_cover():
+@pytest.mark.parametrize("kind", [DOCUMENT, DOCUMENT_BIDIR])
+def test_units_document_order_and_cover(kind):
     cu = np.array([0, 5, 600, 601, 1400, 1400, 1700], dtype=np.int32)
     Hq = 2
-    u = attn.attn_plan_units(DOCUMENT, len(cu) - 1, Hq, int(cu[-1]), cu)
+    u = attn.attn_plan_units(kind, len(cu) - 1, Hq, int(cu[-1]), cu)
     want = [(s, h, t) for s in range(len(cu) - 1) for h in range(Hq)
             for t in range((int(cu[s + 1] - cu[s]) + 255) // 256)]
     assert sorted(u) == sorted(want)

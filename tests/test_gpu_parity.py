@@ -131,6 +131,60 @@ def test_document_ragged(d, lens):
 
 
 @pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("W", [0, 1, 2, 127, 128, 129, 300, 1000])
+def test_sliding_bidir_ragged(d, W):
+    w = I.dense_workload(600 + W, 1, 4, 2, 777, d, I.MASK_SLIDING_BIDIR, window=W)
+    compare(w, run(w), strict=False)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("P", [0, 1, 100, 128, 129, 500, 777, 1000])
+def test_prefix_lm_ragged(d, P):
+    w = I.dense_workload(700 + P, 1, 4, 2, 777, d, I.MASK_PREFIX_LM, window=P)
+    compare(w, run(w), strict=False)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("lens", [[1], [2, 1, 127], [129, 256, 1, 300], [600, 5, 257, 128, 384]])
+def test_document_bidir_ragged(d, lens):
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    w = I.document_workload(800 + len(lens), int(cu[-1]), 4, d, cu_seqlens=cu, Hkv=2,
+                            mask_kind=I.MASK_DOCUMENT_BIDIR)
+    compare(w, run(w), strict=False)
+
+
+@pytest.mark.parametrize("cfg", ["3b", "3p"])
+def test_mask_variant_workloads_sampled(cfg):
+    """The two-sided window and prefix-LM workloads at full size, in the launch configuration
+    the benchmark suite times, on sampled rows (both sequence ends, the window and prefix
+    edges, and random rows)."""
+    w = I.config(cfg)
+    dp = run(w)
+    rng = np.random.default_rng(8)
+    n = int(np.prod(w.lse_shape))
+    heads = np.arange(w.B * w.Hq) * w.N
+    rows = np.unique(np.concatenate([rng.integers(0, n, 2000), heads, heads + w.N - 1,
+                                     heads + w.window - 1, heads + w.window,
+                                     heads + w.N - 1 - w.window]))
+    compare(w, dp, rows=rows)
+
+
+def test_document_bidir_workload():
+    w = I.config("4b")
+    compare(w, run(w))
+
+
+def test_bidir_window_covering_equals_none_bit_exact():
+    """A two-sided window reaching every key makes every key tile full, so the kernel does
+    exactly what the unmasked kernel does."""
+    a = I.dense_workload(31, 1, 4, 2, 600, 128, I.MASK_NONE)
+    b = I.dense_workload(31, 1, 4, 2, 600, 128, I.MASK_SLIDING_BIDIR, window=600)
+    ra, rb = run(a), run(b)
+    assert torch.equal(ra.o.view(torch.int16), rb.o.view(torch.int16))
+    assert torch.equal(ra.lse, rb.lse)
+
+
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("group", [1, 2, 4, 8])
 def test_paged_ragged(d, group):
     lens = [1, 63, 64, 65, 1000, 1025, 2048, 3000]

@@ -20,6 +20,9 @@ ATTN_MASK_SLIDING = 2
 ATTN_MASK_DOCUMENT = 3
 ATTN_MASK_PAGED_DECODE = 4
 ATTN_MASK_DECODE = 5
+ATTN_MASK_SLIDING_BIDIR = 6
+ATTN_MASK_DOCUMENT_BIDIR = 7
+ATTN_MASK_PREFIX_LM = 8
 
 ATTN_OK = 0
 ATTN_ERR_INVALID = -1

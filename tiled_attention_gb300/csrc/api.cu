@@ -117,6 +117,23 @@ int encode_3d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, u
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Mask kinds served by the prefill kernel.
+bool prefill_kind(int m) {
+  return m == ATTN_MASK_NONE || m == ATTN_MASK_CAUSAL || m == ATTN_MASK_SLIDING ||
+         m == ATTN_MASK_DOCUMENT || m == ATTN_MASK_SLIDING_BIDIR ||
+         m == ATTN_MASK_DOCUMENT_BIDIR || m == ATTN_MASK_PREFIX_LM;
+}
+
+bool document_kind(int m) { return m == ATTN_MASK_DOCUMENT || m == ATTN_MASK_DOCUMENT_BIDIR; }
+
+// The window argument: SLIDING needs >= 1 key, SLIDING_BIDIR >= 0 keys per side, PREFIX_LM a
+// prefix of >= 0 tokens; the other kinds ignore it.
+bool window_ok(int m, int window) {
+  if (m == ATTN_MASK_SLIDING) return window >= 1;
+  if (m == ATTN_MASK_SLIDING_BIDIR || m == ATTN_MASK_PREFIX_LM) return window >= 0;
+  return true;
+}
+
 constexpr unsigned long long kTimeoutNs = 2000000000ull;  // 2 s per pipeline wait
 constexpr int kDecodeChunkPages = 16;
 constexpr int kDecodePage = 64;  // tokens per page (the pool's, or 64-row slices of a cache)
@@ -230,7 +247,7 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
              int num_pages, void* workspace, size_t workspace_bytes, void* stream_) {
   g_last_error.clear();
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
-  if (mask_kind < ATTN_MASK_NONE || mask_kind > ATTN_MASK_DECODE)
+  if (mask_kind < ATTN_MASK_NONE || mask_kind > ATTN_MASK_PREFIX_LM)
     return fail(ATTN_ERR_INVALID, "unknown mask_kind %d", mask_kind);
   const bool decode = mask_kind == ATTN_MASK_PAGED_DECODE || mask_kind == ATTN_MASK_DECODE;
   if (B < 0 || N < 0 || Hq <= 0 || Hkv <= 0)
@@ -239,9 +256,9 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
   if (d != 64 && d != 128) return fail(ATTN_ERR_UNSUPPORTED, "head dim %d (64 or 128)", d);
   if (!std::isfinite(scale)) return fail(ATTN_ERR_INVALID, "scale is not finite");
   if (!(scale > 0.f)) return fail(ATTN_ERR_UNSUPPORTED, "scale must be > 0");
-  if (mask_kind == ATTN_MASK_SLIDING && window < 1)
-    return fail(ATTN_ERR_INVALID, "window %d < 1", window);
-  if ((mask_kind == ATTN_MASK_DOCUMENT || decode) && !cu_seqlens)
+  if (!window_ok(mask_kind, window))
+    return fail(ATTN_ERR_INVALID, "window %d out of range for mask_kind %d", window, mask_kind);
+  if ((document_kind(mask_kind) || decode) && !cu_seqlens)
     return fail(ATTN_ERR_INVALID, "cu_seqlens is required");
   if (B == 0 || N == 0) return ATTN_OK;  // nothing to compute
   if (!q || !k || !v || !o || !lse) return fail(ATTN_ERR_INVALID, "null tensor pointer");
@@ -270,7 +287,7 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
   } else {
     if (static_cast<long long>(B) * Hq >= (1ll << 31))
       return fail(ATTN_ERR_UNSUPPORTED, "B*Hq too large");
-    const long long units = mask_kind == ATTN_MASK_DOCUMENT
+    const long long units = document_kind(mask_kind)
                                 ? static_cast<long long>(Hq) * (N / kUnitRows + B)
                                 : static_cast<long long>(B) * Hq * pairs_for_rows(N);
     if (units >= (1ll << 31) - 1) return fail(ATTN_ERR_UNSUPPORTED, "too many work units");
@@ -321,9 +338,9 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
 
   // Prefill kinds. For DOCUMENT the unit count is an upper bound (the segment lengths live
   // on the device): units past the real end decode invalid and end a CTA's loop.
-  const int planes_q = mask_kind == ATTN_MASK_DOCUMENT ? Hq : B * Hq;
-  const int planes_kv = mask_kind == ATTN_MASK_DOCUMENT ? Hkv : B * Hkv;
-  const long long units = mask_kind == ATTN_MASK_DOCUMENT
+  const int planes_q = document_kind(mask_kind) ? Hq : B * Hq;
+  const int planes_kv = document_kind(mask_kind) ? Hkv : B * Hkv;
+  const long long units = document_kind(mask_kind)
                               ? static_cast<long long>(Hq) * (N / kUnitRows + B)
                               : static_cast<long long>(B) * Hq * pairs_for_rows(N);
   CUtensorMap tq, tk, tv, to;
@@ -407,8 +424,8 @@ void attn_release(void) {
 
 int attn_plan_kv_range(int mask_kind, int window, int r0, int bm, int row_end, int k_org,
                        int k_end, int bn, int* lo, int* hi) {
-  if (!lo || !hi || bm <= 0 || bn <= 0 || mask_kind < 0 || mask_kind > ATTN_MASK_DOCUMENT ||
-      (mask_kind == ATTN_MASK_SLIDING && window < 1))
+  if (!lo || !hi || bm <= 0 || bn <= 0 || !prefill_kind(mask_kind) ||
+      !window_ok(mask_kind, window))
     return ATTN_ERR_INVALID;
   const KvRange r = kv_tile_range(mask_kind, window, r0, bm, row_end, k_org, k_end, bn);
   *lo = r.lo;
@@ -418,18 +435,16 @@ int attn_plan_kv_range(int mask_kind, int window, int r0, int bm, int row_end, i
 
 int attn_plan_tile_kind(int mask_kind, int window, int r0, int bm, int row_end, int k_org,
                         int k_end, int bn, int t) {
-  if (bm <= 0 || bn <= 0 || mask_kind < 0 || mask_kind > ATTN_MASK_DOCUMENT ||
-      (mask_kind == ATTN_MASK_SLIDING && window < 1))
+  if (bm <= 0 || bn <= 0 || !prefill_kind(mask_kind) || !window_ok(mask_kind, window))
     return ATTN_ERR_INVALID;
   return tile_kind(mask_kind, window, r0, bm, row_end, k_org, k_end, bn, t);
 }
 
 int attn_plan_units(int mask_kind, int B, int Hq, int N, const int32_t* cu, int32_t* out,
                     int max_units) {
-  if (B < 0 || Hq <= 0 || N < 0 || mask_kind < 0 || mask_kind > ATTN_MASK_DOCUMENT)
-    return ATTN_ERR_INVALID;
+  if (B < 0 || Hq <= 0 || N < 0 || !prefill_kind(mask_kind)) return ATTN_ERR_INVALID;
   std::vector<int32_t> units;
-  if (mask_kind != ATTN_MASK_DOCUMENT) {
+  if (!document_kind(mask_kind)) {
     const int npairs = pairs_for_rows(N);
     for (int level = npairs - 1; level >= 0; --level)
       for (int b = 0; b < B; ++b)

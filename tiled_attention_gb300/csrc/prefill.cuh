@@ -1,5 +1,5 @@
-// prefill.cuh — fused tiled attention forward for sm_103a (dense, causal, sliding window,
-// document segments).
+// prefill.cuh — fused tiled attention forward for sm_103a (no mask, causal, sliding window
+// one- and two-sided, document segments causal and non-causal, prefix-LM).
 //
 // Work unit: two 128-row query tiles of one (batch or segment, query head). The kernel is
 // persistent, one CTA per SM: CTA b of G takes units b, 2G-1-b, 2G+b, 4G-1-b, ... of the
@@ -47,7 +47,7 @@ struct PrefillParams {
   const int* cu_seqlens;    // DOCUMENT: [B+1]
   int B, Hq, Hkv, N, group; // N: rows per (batch, head) plane (T for DOCUMENT)
   int num_units;            // work units; DOCUMENT: an upper bound (surplus ones decode invalid)
-  int window;
+  int window;               // SLIDING / SLIDING_BIDIR window, PREFIX_LM prefix length
   float scale_log2;         // scale * log2(e)
   int* status;
   unsigned long long timeout_ns;
@@ -103,7 +103,7 @@ template <int MASK>
 __device__ __forceinline__ Unit decode_unit(int u, const PrefillParams& p) {
   Unit r{0, 0, 0, 0, 0, 0};
   const int lane = static_cast<int>(lane_id());
-  if (MASK != kMaskDocument) {
+  if (!is_document(MASK)) {
     const int per_level = p.B * p.Hq;
     const int npairs = pairs_for_rows(p.N);
     if (u >= per_level * npairs) return r;
@@ -462,7 +462,7 @@ __global__ void __launch_bounds__(384, 1)
         if (kind == kTileBoundary) {
           const int key0 = k_org + j * BN;
           const int lo_k = vis_lo(MASK, p.window, k_org, row) - key0;
-          const int hi_k = vis_hi(MASK, k_end, row) - key0;
+          const int hi_k = vis_hi(MASK, p.window, k_end, row) - key0;
 #pragma unroll
           for (int t = 0; t < 32; ++t) {
             if (t < lo_k || t > hi_k) f0[t] = -INFINITY;
@@ -538,7 +538,7 @@ __global__ void __launch_bounds__(384, 1)
       // DOCUMENT warp whose rows run past its segment writes them one thread per row instead,
       // so the next segment's rows stay untouched.
       const int warp_row0 = q_row0 + i * BM + quarter * 32;
-      const bool staged = MASK != kMaskDocument || warp_row0 + 31 < row_end;
+      const bool staged = !is_document(MASK) || warp_row0 + 31 < row_end;
       uint8_t* stage = q_s + (qn % QB) * C::kQBytes;
       uint8_t* orow = static_cast<uint8_t*>(p.o) +
                       (static_cast<size_t>(bh) * p.N + static_cast<size_t>(row)) * D * 2;

@@ -26,6 +26,10 @@ cudaError_t launch_prefill_d128(int mask, const CUtensorMap& q, const CUtensorMa
     case kMaskCausal: return launch_one<kMaskCausal>(q, k, v, o, p, grid, stream);
     case kMaskSliding: return launch_one<kMaskSliding>(q, k, v, o, p, grid, stream);
     case kMaskDocument: return launch_one<kMaskDocument>(q, k, v, o, p, grid, stream);
+    case kMaskSlidingBidir: return launch_one<kMaskSlidingBidir>(q, k, v, o, p, grid, stream);
+    case kMaskDocumentBidir:
+      return launch_one<kMaskDocumentBidir>(q, k, v, o, p, grid, stream);
+    case kMaskPrefixLM: return launch_one<kMaskPrefixLM>(q, k, v, o, p, grid, stream);
     default: return cudaErrorInvalidValue;
   }
 }

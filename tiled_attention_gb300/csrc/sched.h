@@ -8,7 +8,9 @@
 // Tiles of the first kind that are not of the second are the boundary tiles, the only ones
 // that need an element mask ("Optimizing Triton Kernels for Custom Attention Patterns on
 // H100", Pattern B: mask only the first and last key tile; Pattern A: skip the boundary check
-// inside a document). Key tiles holding no visible pair are never loaded or computed.
+// inside a document). Key tiles holding no visible pair are never loaded or computed. The
+// same page names prefix-LM among the masks with this kind of structure; causal, both window
+// forms, both document forms and prefix-LM all give monotone intervals.
 #pragma once
 
 #if defined(__CUDACC__)
@@ -20,7 +22,11 @@
 namespace ta {
 
 enum MaskKind { kMaskNone = 0, kMaskCausal = 1, kMaskSliding = 2, kMaskDocument = 3,
-                kMaskPaged = 4 };
+                kMaskPaged = 4, kMaskDecode = 5, kMaskSlidingBidir = 6, kMaskDocumentBidir = 7,
+                kMaskPrefixLM = 8 };
+
+// Kinds whose rows are packed segments described by cu_seqlens.
+TA_HD bool is_document(int mask) { return mask == kMaskDocument || mask == kMaskDocumentBidir; }
 
 enum TileKind { kTileEmpty = 0, kTileFull = 1, kTileBoundary = 2 };
 
@@ -29,17 +35,26 @@ TA_HD int imax(int a, int b) { return a > b ? a : b; }
 
 // First visible key of query row i; keys are numbered in the same space as rows, and the keys
 // a tile schedule may touch start at k_org (0, or the start of the query's document segment).
+//   SLIDING        i - W < j        (causal window of W keys, the query included)
+//   SLIDING_BIDIR  i - W <= j       (W keys on each side of the query)
 TA_HD int vis_lo(int mask, int window, int k_org, int i) {
-  return mask == kMaskSliding ? imax(k_org, i - window + 1) : k_org;
+  if (mask == kMaskSliding) return imax(k_org, i - window + 1);
+  if (mask == kMaskSlidingBidir) return imax(k_org, i - window);
+  return k_org;
 }
 
-// Last visible key of query row i; keys end before k_end.
-TA_HD int vis_hi(int mask, int k_end, int i) {
-  return mask == kMaskNone ? k_end - 1 : imin(i, k_end - 1);
+// Last visible key of query row i; keys end before k_end. `window` is the two-sided window
+// (SLIDING_BIDIR) or the prefix length P (PREFIX_LM: rows below P see the whole prefix).
+TA_HD int vis_hi(int mask, int window, int k_end, int i) {
+  if (mask == kMaskNone || mask == kMaskDocumentBidir) return k_end - 1;
+  if (mask == kMaskSlidingBidir)  // i + W without overflow for any W >= 0
+    return i > k_end - 1 - window ? k_end - 1 : i + window;
+  if (mask == kMaskPrefixLM) return imin(imax(i, window - 1), k_end - 1);
+  return imin(i, k_end - 1);
 }
 
 TA_HD bool pair_visible(int mask, int window, int k_org, int k_end, int i, int j) {
-  return j >= vis_lo(mask, window, k_org, i) && j <= vis_hi(mask, k_end, i);
+  return j >= vis_lo(mask, window, k_org, i) && j <= vis_hi(mask, window, k_end, i);
 }
 
 struct KvRange {
@@ -54,7 +69,7 @@ TA_HD KvRange kv_tile_range(int mask, int window, int r0, int bm, int row_end, i
   const int r1 = imin(r0 + bm, row_end) - 1;
   if (r1 < r0) return r;
   const int a = vis_lo(mask, window, k_org, r0);
-  const int b = vis_hi(mask, k_end, r1);
+  const int b = vis_hi(mask, window, k_end, r1);
   if (b < a) return r;
   r.lo = (a - k_org) / bn;
   r.hi = (b - k_org) / bn + 1;
@@ -67,8 +82,10 @@ TA_HD int tile_kind(int mask, int window, int r0, int bm, int row_end, int k_org
   if (r1 < r0) return kTileEmpty;
   const int k0 = k_org + t * bn;
   const int k1 = k0 + bn - 1;
-  if (k0 > vis_hi(mask, k_end, r1) || k1 < vis_lo(mask, window, k_org, r0)) return kTileEmpty;
-  if (vis_lo(mask, window, k_org, r1) <= k0 && k1 <= vis_hi(mask, k_end, r0)) return kTileFull;
+  if (k0 > vis_hi(mask, window, k_end, r1) || k1 < vis_lo(mask, window, k_org, r0))
+    return kTileEmpty;
+  if (vis_lo(mask, window, k_org, r1) <= k0 && k1 <= vis_hi(mask, window, k_end, r0))
+    return kTileFull;
   return kTileBoundary;
 }
 

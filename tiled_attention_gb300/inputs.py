@@ -291,4 +291,16 @@ def config(k) -> Workload:
     if k == 5:
         return paged_decode_workload(1005, 32, 1024, 16384, 32, 8, 128, name=(
             "paged decode B32 L U[1024,16384] Hq32 Hkv8 d128 page64"))
+    # The mask variants on the same shapes: a two-sided window with as many keys per query as
+    # the causal window above, a prefix of half the sequence, and config 4's segments without
+    # the causal constraint.
+    if k == "3b":
+        return dense_workload(1003, 2, 32, 8, 8192, 128, MASK_SLIDING_BIDIR, window=2048,
+                              name="two-sided window W2048 B2 Hq32 Hkv8 N8192 d128")
+    if k == "3p":
+        return dense_workload(1003, 2, 32, 8, 8192, 128, MASK_PREFIX_LM, window=4096,
+                              name="prefix-LM P4096 B2 Hq32 Hkv8 N8192 d128")
+    if k == "4b":
+        return document_workload(1004, 16384, 16, 64, 256, 4096, mask_kind=MASK_DOCUMENT_BIDIR,
+                                 name="non-causal document T16384 H16 d64 seg U[256,4096]")
     raise KeyError(k)
