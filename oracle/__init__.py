@@ -43,8 +43,8 @@ def _load(path: str = None):
         p = ctypes.c_void_p
         i = ctypes.c_int
         i64 = ctypes.c_int64
-        lib.oracle_attn.argtypes = [p, p, p, i, i, i, i, i, ctypes.c_float, i, i, p, p, i, i,
-                                    p, i64, p, p, p, i64, i]
+        lib.oracle_attn.argtypes = [p, p, p, i, i, i, i, i, ctypes.c_float, i, i, p, p, p, i,
+                                    i, p, i64, p, p, p, i64, i]
         lib.oracle_attn.restype = i
         lib.oracle_max_threads.argtypes = [i]
         lib.oracle_max_threads.restype = i
@@ -73,6 +73,8 @@ def attention(w, rows=None, probs: bool = False, threads: int = 0, lib_path: str
     v = np.ascontiguousarray(w.v, dtype=np.uint16)
     cu = None if w.cu_seqlens is None else np.ascontiguousarray(w.cu_seqlens, dtype=np.int32)
     tab = None if w.block_table is None else np.ascontiguousarray(w.block_table, dtype=np.int32)
+    lk = getattr(w, "seqlens_k", None)
+    lk = None if lk is None else np.ascontiguousarray(lk, dtype=np.int32)
     max_pages = 0 if tab is None else tab.shape[1]
     total = int(np.prod(w.lse_shape))
     if rows is None:
@@ -83,11 +85,16 @@ def attention(w, rows=None, probs: bool = False, threads: int = 0, lib_path: str
         n = rows_arr.size
     o = np.zeros((n, w.d), dtype=np.float64)
     lse = np.zeros(n, dtype=np.float64)
-    nk = w.N if w.mask_kind not in (4, 5) else int(np.diff(cu).max(initial=0))
+    if w.mask_kind in (4, 5):
+        nk = int(np.diff(cu).max(initial=0))
+    elif lk is not None:
+        nk = max(w.N, int(lk.max(initial=0)))
+    else:
+        nk = w.N
     pr = np.zeros((n, max(nk, 1)), dtype=np.float64) if probs else None
     rc = lib.oracle_attn(_ptr(q), _ptr(k), _ptr(v), w.B, w.Hq, w.Hkv, w.N, w.d,
-                         ctypes.c_float(w.scale), w.mask_kind, w.window, _ptr(cu), _ptr(tab),
-                         max_pages, w.page_size, _ptr(rows_arr), n, _ptr(o), _ptr(lse),
+                         ctypes.c_float(w.scale), w.mask_kind, w.window, _ptr(cu), _ptr(lk),
+                         _ptr(tab), max_pages, w.page_size, _ptr(rows_arr), n, _ptr(o), _ptr(lse),
                          _ptr(pr), pr.shape[1] if probs else 0, threads)
     if rc != 0:
         raise ValueError(f"oracle_attn rejected the problem (code {rc})")

@@ -40,6 +40,12 @@
  *              prefix-LM mask the same page lists among masks with exploitable structure:
  *              the first P tokens see each other in both directions, later tokens see
  *              every earlier token)
+ *   PAGED_PREFILL  a chunk of Lq_b new query tokens of sequence b whose context (the chunk
+ *              included) holds Lk_b >= Lq_b keys in a paged cache: query t of the chunk sits
+ *              at position Lk_b - Lq_b + t and sees keys j <= that position, read through
+ *              the block table as for PAGED (Pattern C's prefix-caching use of a block
+ *              table, with the query block longer than one token). Queries are packed like
+ *              DOCUMENT: cu[] holds the chunks' starts, seqlens_k[] the context lengths.
  *
  * Inputs are raw bf16 bit patterns widened exactly to fp64. The fp32 scale is widened too.
  * A row that sees no key (impossible for valid inputs) gets O = 0 and LSE = -inf.
@@ -53,13 +59,18 @@
 #endif
 
 enum { OR_NONE = 0, OR_CAUSAL = 1, OR_SLIDING = 2, OR_DOCUMENT = 3, OR_PAGED = 4, OR_DECODE = 5,
-       OR_SLIDING_BIDIR = 6, OR_DOCUMENT_BIDIR = 7, OR_PREFIX_LM = 8 };
+       OR_SLIDING_BIDIR = 6, OR_DOCUMENT_BIDIR = 7, OR_PREFIX_LM = 8, OR_PAGED_PREFILL = 9 };
 
 /* One query per sequence (PAGED, DECODE). */
 static int is_decode(int mask) { return mask == OR_PAGED || mask == OR_DECODE; }
 
-/* Packed segments described by cu_seqlens (DOCUMENT, DOCUMENT_BIDIR). */
-static int is_document(int mask) { return mask == OR_DOCUMENT || mask == OR_DOCUMENT_BIDIR; }
+/* Packed query rows described by cu_seqlens (DOCUMENT, DOCUMENT_BIDIR, PAGED_PREFILL). */
+static int is_document(int mask) {
+    return mask == OR_DOCUMENT || mask == OR_DOCUMENT_BIDIR || mask == OR_PAGED_PREFILL;
+}
+
+/* Keys read through a block table. */
+static int is_paged(int mask) { return mask == OR_PAGED || mask == OR_PAGED_PREFILL; }
 
 typedef struct {
     const uint16_t *q, *k, *v;
@@ -67,6 +78,7 @@ typedef struct {
     double s;
     int mask, W;
     const int32_t *cu;
+    const int32_t *seqlens_k;
     const int32_t *table;
     int max_pages, page;
 } problem_t;
@@ -107,6 +119,7 @@ static void row_coords(const problem_t *P, int64_t r, int *b, int *h, int *i) {
 /* Number of keys row i of batch b can address (before the mask). */
 static int key_count(const problem_t *P, int b) {
     if (is_decode(P->mask)) return P->cu[b + 1] - P->cu[b];
+    if (P->mask == OR_PAGED_PREFILL) return P->seqlens_k[b];
     return P->N;
 }
 
@@ -121,6 +134,10 @@ static int visible(const problem_t *P, int b, int i, int j) {
     case OR_SLIDING_BIDIR: return (int64_t)j >= (int64_t)i - P->W && (int64_t)j <= (int64_t)i + P->W;
     case OR_DOCUMENT_BIDIR: return j >= P->cu[b] && j < P->cu[b + 1];
     case OR_PREFIX_LM: return j <= i || j < P->W;
+    case OR_PAGED_PREFILL: {
+        const int Lq = P->cu[b + 1] - P->cu[b], Lk = P->seqlens_k[b];
+        return j < Lk && j <= (i - P->cu[b]) + (Lk - Lq);
+    }
     }
     return 0;
 }
@@ -133,7 +150,7 @@ static const uint16_t *query_row(const problem_t *P, int b, int h, int i) {
 
 /* Key or value row j of (b, g); base is the k or the v tensor. */
 static const uint16_t *kv_row(const problem_t *P, const uint16_t *base, int b, int g, int j) {
-    if (P->mask == OR_PAGED) {
+    if (is_paged(P->mask)) {
         int phys = P->table[(size_t)b * P->max_pages + j / P->page];
         return base + ((((size_t)phys * P->Hkv + g) * P->page) + (size_t)(j % P->page)) * P->d;
     }
@@ -193,13 +210,14 @@ static void attend_row(const problem_t *P, int64_t r, double *z, double *o, doub
  */
 int oracle_attn(const uint16_t *q, const uint16_t *k, const uint16_t *v, int B, int Hq,
                 int Hkv, int N, int d, float scale, int mask_kind, int window,
-                const int32_t *cu_seqlens, const int32_t *block_table, int max_pages,
-                int page_size, const int64_t *rows, int64_t nrows, double *o, double *lse,
-                double *probs, int64_t probs_stride, int nthreads) {
+                const int32_t *cu_seqlens, const int32_t *seqlens_k,
+                const int32_t *block_table, int max_pages, int page_size, const int64_t *rows,
+                int64_t nrows, double *o, double *lse, double *probs, int64_t probs_stride,
+                int nthreads) {
     problem_t P = {q, k, v, B, Hq, Hkv, N, d, (double)scale, mask_kind, window,
-                   cu_seqlens, block_table, max_pages, page_size};
+                   cu_seqlens, seqlens_k, block_table, max_pages, page_size};
     if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || d <= 0 || N < 0) return -1;
-    if (mask_kind < OR_NONE || mask_kind > OR_PREFIX_LM) return -1;
+    if (mask_kind < OR_NONE || mask_kind > OR_PAGED_PREFILL) return -1;
     if (mask_kind == OR_SLIDING && window < 1) return -1;
     if ((mask_kind == OR_SLIDING_BIDIR || mask_kind == OR_PREFIX_LM) && window < 0) return -1;
     if ((is_document(mask_kind) || is_decode(mask_kind)) && !cu_seqlens) return -1;
@@ -207,7 +225,14 @@ int oracle_attn(const uint16_t *q, const uint16_t *k, const uint16_t *v, int B, 
         const int L = cu_seqlens[b + 1] - cu_seqlens[b];
         if (L < 0 || L > N) return -1;  /* the dense cache holds N keys per sequence */
     }
-    if (mask_kind == OR_PAGED && (!block_table || page_size <= 0)) return -1;
+    if (is_paged(mask_kind) && (!block_table || page_size <= 0)) return -1;
+    if (mask_kind == OR_PAGED_PREFILL) {
+        if (!seqlens_k || cu_seqlens[0] != 0 || cu_seqlens[B] != N) return -1;
+        for (int b = 0; b < B; b++) {
+            const int Lq = cu_seqlens[b + 1] - cu_seqlens[b], Lk = seqlens_k[b];
+            if (Lq < 0 || Lk < Lq || Lk > max_pages * page_size) return -1;
+        }
+    }
 
     const int64_t total = row_count(&P);
     const int64_t n = rows ? nrows : total;
@@ -218,6 +243,8 @@ int oracle_attn(const uint16_t *q, const uint16_t *k, const uint16_t *v, int B, 
         int L = cu_seqlens[b + 1] - cu_seqlens[b];
         if (L > maxk) maxk = L;
     }
+    for (int b = 0; mask_kind == OR_PAGED_PREFILL && b < B; b++)
+        if (seqlens_k[b] > maxk) maxk = seqlens_k[b];
     if (probs && probs_stride < maxk) return -1;
 
 #ifdef _OPENMP

@@ -17,7 +17,7 @@ from tiled_attention_gb300 import inputs as I
 GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
 
 KINDS = ["none", "causal", "sliding", "document", "paged", "decode", "sliding_bidir",
-         "document_bidir", "prefix_lm"]
+         "document_bidir", "prefix_lm", "paged_prefill"]
 
 
 def widen(bits):
@@ -52,6 +52,10 @@ def tiny(kind: str, seed: int = 7, window: int = 5):
     if kind == "prefix_lm":
         return I.dense_workload(seed, 2, 4, 2, 37, 16, I.MASK_PREFIX_LM,
                                 window=9 if window == 5 else window)
+    if kind == "paged_prefill":
+        return I.paged_prefill_workload(seed, 4, 0, 0, 0, 0, 4, 2, 16, page_size=8,
+                                        spare_pages=3, context_lens=[1, 40, 130, 9],
+                                        chunk_lens=[1, 17, 33, 9])
     raise KeyError(kind)
 
 
@@ -91,6 +95,18 @@ def dense_problems(w):
         for h in range(w.Hq):
             rows = h * T + np.arange(T)
             yield rows, qf[0, h], kf[0, h // group], vf[0, h // group], mask.numpy()
+    elif w.mask_kind == I.MASK_PAGED_PREFILL:
+        P = w.page_size
+        for b in range(w.B):
+            a, e = int(w.cu_seqlens[b]), int(w.cu_seqlens[b + 1])
+            Lq, Lk = e - a, int(w.seqlens_k[b])
+            pages = [int(w.block_table[b, p]) for p in range((Lk + P - 1) // P)]
+            mask = torch.tril(torch.ones(Lq, Lk, dtype=torch.bool), diagonal=Lk - Lq).numpy()
+            for h in range(w.Hq):
+                g = h // group
+                kk = np.concatenate([kf[p, g] for p in pages], axis=0)[:Lk]
+                vv = np.concatenate([vf[p, g] for p in pages], axis=0)[:Lk]
+                yield h * w.N + np.arange(a, e), qf[0, h, a:e], kk, vv, mask
     elif w.mask_kind == I.MASK_DECODE:
         for b in range(w.B):
             L = int(w.cu_seqlens[b + 1] - w.cu_seqlens[b])
@@ -177,6 +193,16 @@ def _set_dominant(w, r, jstar):
         g = h // group
         w.q[b, h, 0, :] = 0
         w.q[b, h, 0, 0] = bf16(32.0)
+        w.k[:, g, :, 0] = 0
+        P = w.page_size
+        w.k[w.block_table[b, jstar // P], g, jstar % P, 0] = bf16(32.0)
+        return
+    if w.mask_kind == I.MASK_PAGED_PREFILL:
+        h, i = divmod(r, w.N)
+        b = int(np.searchsorted(w.cu_seqlens, i, side="right")) - 1
+        g = h // group
+        w.q[0, h, i, :] = 0
+        w.q[0, h, i, 0] = bf16(32.0)
         w.k[:, g, :, 0] = 0
         P = w.page_size
         w.k[w.block_table[b, jstar // P], g, jstar % P, 0] = bf16(32.0)
@@ -310,6 +336,10 @@ def pin_gqa_equals_repeated_mha(attn, kind):
         m.block_table = w.block_table.copy()
     elif kind == "decode":
         m = I.dense_decode_workload(7, 3, 0, 0, 4, 4, 16, N=137, context_lens=[1, 63, 130])
+    elif kind == "paged_prefill":
+        m = I.paged_prefill_workload(7, 4, 0, 0, 0, 0, 4, 4, 16, page_size=8, spare_pages=3,
+                                     context_lens=[1, 40, 130, 9], chunk_lens=[1, 17, 33, 9])
+        m.block_table = w.block_table.copy()
     elif kind in ("document", "document_bidir"):
         m = I.document_workload(7, 37, 4, 16, cu_seqlens=[0, 5, 6, 20, 37], Hkv=4,
                                 mask_kind=w.mask_kind)
@@ -393,6 +423,51 @@ def pin_document_bidir_segments(attn):
     d.q[...], d.k[...], d.v[...] = n.q, n.k, n.v
     assert np.array_equal(attn(d)[0], attn(n)[0])
     assert np.array_equal(attn(d)[1], attn(n)[1])
+
+
+def pin_paged_prefill_whole_context_equals_document(attn):
+    """A chunk that is the whole context is causal attention over that sequence: the same as
+    the causal document mask over the gathered tokens, bit for bit."""
+    lens = [1, 40, 130, 9]
+    w = I.paged_prefill_workload(17, 4, 0, 0, 0, 0, 4, 2, 16, page_size=8, spare_pages=3,
+                                 context_lens=lens, chunk_lens=lens)
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    d = I.document_workload(0, int(cu[-1]), 4, 16, cu_seqlens=cu, Hkv=2)
+    d.q[...] = w.q
+    P = w.page_size
+    for b, L in enumerate(lens):
+        pages = [int(w.block_table[b, p]) for p in range((L + P - 1) // P)]
+        d.k[0, :, cu[b]:cu[b + 1]] = np.concatenate([w.k[p] for p in pages], axis=1)[:, :L]
+        d.v[0, :, cu[b]:cu[b + 1]] = np.concatenate([w.v[p] for p in pages], axis=1)[:, :L]
+    assert np.array_equal(attn(w)[0], attn(d)[0])
+    assert np.array_equal(attn(w)[1], attn(d)[1])
+
+
+def pin_paged_prefill_last_row_equals_decode(attn):
+    """The last row of each chunk sees the whole context: it is the paged decode of that
+    sequence with the same pool and block table, bit for bit."""
+    w = tiny("paged_prefill")
+    o, lse = attn(w)
+    dec = I.paged_decode_workload(0, w.B, 0, 0, w.Hq, w.Hkv, w.d, page_size=w.page_size,
+                                  spare_pages=3, context_lens=w.seqlens_k)
+    dec.k, dec.v, dec.block_table = w.k, w.v, w.block_table
+    for b in range(w.B):
+        dec.q[b, :, 0] = w.q[0, :, w.cu_seqlens[b + 1] - 1]
+    od, ld = attn(dec)
+    for b in range(w.B):
+        rows = np.arange(w.Hq) * w.N + (w.cu_seqlens[b + 1] - 1)
+        assert np.array_equal(od[b * w.Hq:(b + 1) * w.Hq], o[rows])
+        assert np.array_equal(ld[b * w.Hq:(b + 1) * w.Hq], lse[rows])
+
+
+def pin_paged_prefill_page_size_invariant(attn):
+    """The same tokens in pools of 8- and 16-token pages (different permutations) give the
+    same results bit for bit."""
+    kw = dict(context_lens=[1, 40, 130, 9], chunk_lens=[1, 17, 33, 9], spare_pages=3)
+    a = I.paged_prefill_workload(19, 4, 0, 0, 0, 0, 4, 2, 16, page_size=8, **kw)
+    b = I.paged_prefill_workload(19, 4, 0, 0, 0, 0, 4, 2, 16, page_size=16, **kw)
+    assert np.array_equal(attn(a)[0], attn(b)[0])
+    assert np.array_equal(attn(a)[1], attn(b)[1])
 
 
 def pin_paged_equals_dense_last_row(attn):
@@ -483,6 +558,8 @@ def all_pins():
     for f in (pin_key_permutation, pin_window_covering_equals_causal,
               pin_single_segment_equals_causal, pin_paged_equals_dense_last_row,
               pin_dense_decode_equals_paged, pin_bidir_window_limits, pin_prefix_limits,
-              pin_document_bidir_segments, pin_closed_form_golden):
+              pin_document_bidir_segments, pin_paged_prefill_whole_context_equals_document,
+              pin_paged_prefill_last_row_equals_decode, pin_paged_prefill_page_size_invariant,
+              pin_closed_form_golden):
         pins.append((f.__name__, f))
     return pins

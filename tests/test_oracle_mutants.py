@@ -42,6 +42,11 @@ MUTANTS = [
      "case OR_PREFIX_LM: return j <= i || j <= P->W;"),
     ("prefix_ignored", "case OR_PREFIX_LM: return j <= i || j < P->W;",
      "case OR_PREFIX_LM: return j <= i;"),
+    ("paged_prefill_no_offset",
+     "return j < Lk && j <= (i - P->cu[b]) + (Lk - Lq);", "return j < Lk && j <= (i - P->cu[b]);"),
+    ("paged_prefill_strict",
+     "return j < Lk && j <= (i - P->cu[b]) + (Lk - Lq);",
+     "return j < Lk && j < (i - P->cu[b]) + (Lk - Lq);"),
     ("query_transposed", "return P->q + (((size_t)b * P->Hq + h) * P->N + i) * P->d;",
      "return P->q + (((size_t)b * P->Hq + h) * P->N) * P->d + i;"),
 ]

@@ -50,7 +50,8 @@ def test_workload_pair_counts():
                     ("sliding_bidir", tiny("sliding_bidir", window=40)),
                     ("document_bidir", tiny("document_bidir")),
                     ("prefix_lm", tiny("prefix_lm")),
-                    ("prefix_lm", tiny("prefix_lm", window=50))]:
+                    ("prefix_lm", tiny("prefix_lm", window=50)),
+                    ("paged_prefill", tiny("paged_prefill"))]:
         _, _, p = oracle.attention(w, probs=True)
         per_head = (p > 0).sum() / w.Hq
         if kind == "document":

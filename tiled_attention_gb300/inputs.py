@@ -29,8 +29,11 @@ MASK_DECODE = 5
 MASK_SLIDING_BIDIR = 6
 MASK_DOCUMENT_BIDIR = 7
 MASK_PREFIX_LM = 8
+# Chunked prefill over a paged cache: served by attn_fwd_paged_prefill, not attn_fwd.
+MASK_PAGED_PREFILL = 9
 DECODE_KINDS = (MASK_PAGED_DECODE, MASK_DECODE)
 DOCUMENT_KINDS = (MASK_DOCUMENT, MASK_DOCUMENT_BIDIR)
+PACKED_KINDS = (MASK_DOCUMENT, MASK_DOCUMENT_BIDIR, MASK_PAGED_PREFILL)
 
 PAGE_SIZE = 64
 # Poison written into unused page slots and spare pages: finite, and large enough that any
@@ -84,6 +87,9 @@ class Workload:
     PAGED_DECODE: q, o ``[B,Hq,1,d]``; k, v pools ``[num_pages,Hkv,64,d]``;
     lse ``[B,Hq]``; N is the longest context.
     DECODE: q, o ``[B,Hq,1,d]``; k, v dense caches ``[B,Hkv,N,d]``; lse ``[B,Hq]``.
+    PAGED_PREFILL: B sequences; query chunks packed ``[1,Hq,N,d]`` with chunk starts in
+    cu_seqlens; k, v pools ``[num_pages,Hkv,page,d]``; seqlens_k holds each sequence's context
+    length (its chunk included); lse ``[1,Hq,N]``.
     """
 
     name: str
@@ -101,12 +107,13 @@ class Workload:
     cu_seqlens: Optional[np.ndarray] = None
     block_table: Optional[np.ndarray] = None
     page_size: int = 0
+    seqlens_k: Optional[np.ndarray] = None
 
     @property
     def out_shape(self):
         if self.mask_kind in DECODE_KINDS:
             return (self.B, self.Hq, 1, self.d)
-        if self.mask_kind in DOCUMENT_KINDS:
+        if self.mask_kind in PACKED_KINDS:
             return (1, self.Hq, self.N, self.d)
         return (self.B, self.Hq, self.N, self.d)
 
@@ -139,6 +146,10 @@ class Workload:
             return lens * (lens + 1) // 2
         if self.mask_kind == MASK_DOCUMENT_BIDIR:
             return lens * lens
+        if self.mask_kind == MASK_PAGED_PREFILL:
+            lk = self.seqlens_k.astype(np.int64)
+            # chunk row t sees lk - lq + t + 1 keys
+            return lens * (lk - lens) + lens * (lens + 1) // 2
         return lens  # decode: one query row sees all L_b keys
 
     def flops(self) -> float:
@@ -147,7 +158,8 @@ class Workload:
 
     def kv_bytes_valid(self) -> int:
         """Decode: K+V bytes of the valid tokens (what an ideal kernel reads)."""
-        lens = np.diff(self.cu_seqlens.astype(np.int64))
+        lens = (self.seqlens_k.astype(np.int64) if self.seqlens_k is not None
+                else np.diff(self.cu_seqlens.astype(np.int64)))
         return int(lens.sum()) * self.Hkv * self.d * 2 * 2
 
 
@@ -236,6 +248,69 @@ def paged_decode_workload(seed: int, B: int, Lmin: int, Lmax: int, Hq: int, Hkv:
     return Workload(name or "paged_decode", MASK_PAGED_DECODE, B, Hq, Hkv, N, d,
                     default_scale(d), q, k_pool, v_pool, cu_seqlens=cu, block_table=table,
                     page_size=page_size)
+
+
+def _paged_pool(rng, lens, Hkv, d, page_size, spare_pages, shuffle):
+    """Token-major K / V for the given context lengths laid out in a permuted page pool.
+    Returns (k_pool, v_pool, block_table). Draws K, V, then the permutation."""
+    B = len(lens)
+    tot = int(lens.sum())
+    k_all = normal_bf16(rng, (Hkv, tot, d)) if tot else np.zeros((Hkv, 0, d), np.uint16)
+    v_all = normal_bf16(rng, (Hkv, tot, d)) if tot else np.zeros((Hkv, 0, d), np.uint16)
+    pages_per_seq = (lens + page_size - 1) // page_size
+    used = int(pages_per_seq.sum())
+    num_pages = used + spare_pages
+    perm = rng.permutation(num_pages) if shuffle else np.arange(num_pages)
+    pk = f32_to_bf16_bits(np.float32(POISON_K))
+    pv = f32_to_bf16_bits(np.float32(POISON_V))
+    k_pool = np.full((num_pages, Hkv, page_size, d), pk, dtype=np.uint16)
+    v_pool = np.full((num_pages, Hkv, page_size, d), pv, dtype=np.uint16)
+    max_pages = int(pages_per_seq.max()) if B else 0
+    table = np.full((B, max(max_pages, 1)), -1, dtype=np.int32)
+    idx = 0
+    tok_phys = np.empty(tot, dtype=np.int64)
+    tok_slot = np.empty(tot, dtype=np.int64)
+    tok0 = 0
+    for b in range(B):
+        np_b = int(pages_per_seq[b])
+        table[b, :np_b] = perm[idx: idx + np_b]
+        idx += np_b
+        t = np.arange(int(lens[b]))
+        tok_phys[tok0: tok0 + len(t)] = table[b, t // page_size]
+        tok_slot[tok0: tok0 + len(t)] = t % page_size
+        tok0 += int(lens[b])
+    k_pool[tok_phys, :, tok_slot, :] = k_all.transpose(1, 0, 2)
+    v_pool[tok_phys, :, tok_slot, :] = v_all.transpose(1, 0, 2)
+    return k_pool, v_pool, table
+
+
+def paged_prefill_workload(seed: int, B: int, Lk_min: int, Lk_max: int, Lq_min: int,
+                           Lq_max: int, Hq: int, Hkv: int, d: int, page_size: int = 16,
+                           spare_pages: int = 64, context_lens=None, chunk_lens=None,
+                           shuffle: bool = True, name: str = "") -> Workload:
+    """Chunked prefill over a paged cache: sequence b's context of Lk_b tokens (uniform in
+    [Lk_min, Lk_max]) sits in a permuted page pool, and its last Lq_b tokens (uniform in
+    [Lq_min, min(Lq_max, Lk_b)]) are the new query chunk. Draw order: context lengths, chunk
+    lengths, Q (packed chunks), K, V, page permutation. Pool slots past each context and the
+    spare pages hold poison; block-table padding is -1."""
+    rng = np.random.default_rng(seed)
+    if context_lens is None:
+        lk = rng.integers(Lk_min, Lk_max + 1, size=B).astype(np.int64)
+    else:
+        lk = np.asarray(context_lens, dtype=np.int64)
+    if chunk_lens is None:
+        lq = np.array([rng.integers(min(Lq_min, L), min(Lq_max, L) + 1) for L in lk],
+                      dtype=np.int64)
+    else:
+        lq = np.asarray(chunk_lens, dtype=np.int64)
+    assert np.all(lq <= lk) and np.all(lq >= 0)
+    T = int(lq.sum())
+    q = normal_bf16(rng, (1, Hq, T, d))
+    k_pool, v_pool, table = _paged_pool(rng, lk, Hkv, d, page_size, spare_pages, shuffle)
+    cu = np.concatenate([[0], np.cumsum(lq)]).astype(np.int32)
+    return Workload(name or "paged_prefill", MASK_PAGED_PREFILL, B, Hq, Hkv, T, d,
+                    default_scale(d), q, k_pool, v_pool, cu_seqlens=cu, block_table=table,
+                    page_size=page_size, seqlens_k=lk.astype(np.int32))
 
 
 def dense_decode_workload(seed: int, B: int, Lmin: int, Lmax: int, Hq: int, Hkv: int, d: int,
