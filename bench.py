@@ -260,7 +260,7 @@ def suite(args):
             line.update(extra)
         print(json.dumps(line), flush=True)
 
-    for cfg in (1, 2, 3, "3c", 4, "3b", "3p", "4b", 5):
+    for cfg in (1, 2, 3, "3c", 4, "3b", "3p", "4b", "6", "6p64", 5, "5p16"):
         w = I.config(cfg)
         dp = DeviceProblem(w, device=dev, fill_outputs=0.0)
         emit(w, timed(lambda: dp.run(stream), args.steps))

@@ -59,7 +59,10 @@ enum attn_mask_kind {
     ATTN_MASK_DECODE = 5,
     ATTN_MASK_SLIDING_BIDIR = 6,
     ATTN_MASK_DOCUMENT_BIDIR = 7,
-    ATTN_MASK_PREFIX_LM = 8
+    ATTN_MASK_PREFIX_LM = 8,
+    /* Chunked prefill over a paged cache: only attn_fwd_paged_prefill takes it (attn_fwd
+     * returns ATTN_ERR_INVALID); attn_plan_units plans it. */
+    ATTN_MASK_PAGED_PREFILL = 9
 };
 
 enum attn_status {
@@ -105,7 +108,7 @@ enum attn_status {
  * block_table int32 device array [B, ceil(N/page_size)]: physical page of logical page p of
  *           sequence b; entries past a sequence's last page are ignored (-1 by convention).
  *           PAGED_DECODE only.
- * page_size tokens per page; PAGED_DECODE supports 64.
+ * page_size tokens per page; PAGED_DECODE supports 16, 32, 64 and 128.
  * num_pages pages in the k / v pools (PAGED_DECODE; bounds-checked on the device).
  *           block_table, page_size and num_pages are ignored for DECODE.
  * workspace device scratch of at least attn_workspace_bytes(...) bytes (may be NULL when that
@@ -117,6 +120,40 @@ int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse, i
              int Hkv, int N, int d, float scale, int mask_kind, int window,
              const int32_t *cu_seqlens, const int32_t *block_table, int page_size,
              int num_pages, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * attn_fwd_paged_prefill — chunked prefill (or prefix reuse) over a paged KV cache.
+ *
+ * Sequence b holds a context of Lk_b = seqlens_k[b] tokens in a page pool; its last Lq_b
+ * tokens are the new query chunk, whose own keys and values are already in the pool. Chunk row
+ * t sits at position Lk_b - Lq_b + t and attends to the context keys j <= Lk_b - Lq_b + t:
+ * causal attention aligned to the end of the context. This is the block-table indirection of
+ * "Optimizing Triton Kernels for Custom Attention Patterns on H100", Pattern C (whose use
+ * cases include prefix caching), with a query block longer than one token. Keys are gathered
+ * page by page through the block table inside the kernel; no dense copy is made.
+ *
+ * q, o      bf16 [1, Hq, total_q, d]: the chunks packed back to back.
+ * lse       fp32 [1, Hq, total_q] (natural log, as for attn_fwd).
+ * k, v      bf16 page pools [num_pages, Hkv, page_size, d].
+ * cu_seqlens_q int32 device array [B+1]: chunk starts, cu[0] = 0, nondecreasing,
+ *           cu[B] = total_q.
+ * seqlens_k int32 device array [B]: context lengths, Lq_b <= Lk_b <= max_pages * page_size.
+ *           Checked on the device with cu_seqlens_q (status ATTN_ERR_SEQLENS, nothing computed).
+ * block_table int32 device array [B, max_pages]: physical page of logical page p of sequence
+ *           b. Only entries p < ceil(Lk_b / page_size) are read; an entry outside
+ *           [0, num_pages) is never dereferenced (status ATTN_ERR_BOUNDS, that page reads as
+ *           zeros).
+ * page_size 16, 32, 64 or 128 (else ATTN_ERR_UNSUPPORTED).
+ * d         64 or 128. Hq % Hkv == 0; query head h reads kv head h / (Hq / Hkv).
+ * Pool slots of a sequence's last page past Lk_b must hold finite values (their
+ * probabilities are exactly zero, and zero times a non-finite value is not zero).
+ * No workspace; asynchronous on `stream`; the caller owns every buffer.
+ */
+int attn_fwd_paged_prefill(const void *q, const void *k, const void *v, void *o, float *lse,
+                           int B, int Hq, int Hkv, int total_q, int d, float scale,
+                           const int32_t *cu_seqlens_q, const int32_t *seqlens_k,
+                           const int32_t *block_table, int max_pages, int page_size,
+                           int num_pages, void *stream);
 
 /* Bytes of workspace attn_fwd needs for these arguments (0 for the prefill kinds; DECODE
  * ignores page_size). */
@@ -200,7 +237,9 @@ int attn_plan_tile_kind(int mask_kind, int window, int r0, int bm, int row_end, 
  * tiles of one (batch or segment, query head); units are ordered longest-first (pair index
  * descending), then by batch/segment, then head, so the heaviest causal tiles start first and
  * heads sharing a kv head run side by side. cu_seqlens is a HOST array here (document kinds
- * only).
+ * only). For ATTN_MASK_PAGED_PREFILL it holds the B+1 chunk starts followed by the B context
+ * lengths, the pair index counts within the chunk, and units are ordered by pair index plus
+ * (context - chunk) / (2*bm) descending, so the chunks with the longest contexts start first.
  * Writes up to max_units records of 3 ints (segment or batch, head, pair index) to out and
  * returns the unit count (or a negative ATTN_ERR_*).
  */

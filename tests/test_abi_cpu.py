@@ -94,6 +94,55 @@ def test_decode_validation_before_cuda():
                   num_pages=4, **base) == attn.ATTN_ERR_INVALID)
 
 
+def _paged_prefill(**kw):
+    t = _FakeDevicePtr()
+    a = dict(q=t, k=t, v=t, o=t, lse=t, B=2, Hq=4, Hkv=2, total_q=300, d=128, scale=0.125,
+             cu_seqlens_q=t, seqlens_k=t, block_table=t, max_pages=8, page_size=16,
+             num_pages=40, stream=0)
+    a.update(kw)
+    return attn.attn_fwd_paged_prefill(**a)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(page_size=48), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(page_size=8), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(d=96), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(Hq=3), attn.ATTN_ERR_INVALID),
+    (dict(scale=-0.5), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(block_table=None), attn.ATTN_ERR_INVALID),
+    (dict(seqlens_k=None), attn.ATTN_ERR_INVALID),
+    (dict(max_pages=0), attn.ATTN_ERR_INVALID),
+    (dict(num_pages=0), attn.ATTN_ERR_INVALID),
+    (dict(num_pages=2**30, Hkv=4, Hq=4), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(q=_FakeDevicePtr(1 << 20 | 8)), attn.ATTN_ERR_INVALID),  # misaligned
+])
+def test_paged_prefill_validation_before_cuda(kw, code):
+    assert _paged_prefill(**kw) == code
+    assert attn.last_error()
+
+
+def test_paged_prefill_empty_is_a_no_op():
+    assert _paged_prefill(B=0) == attn.ATTN_OK
+    assert _paged_prefill(total_q=0) == attn.ATTN_OK
+
+
+def test_attn_fwd_rejects_paged_prefill_kind():
+    assert _call(mask_kind=attn.ATTN_MASK_PAGED_PREFILL) == attn.ATTN_ERR_INVALID
+
+
+def test_paged_decode_page_sizes():
+    t = _FakeDevicePtr()
+    base = dict(q=t, k=t, v=t, o=t, lse=t, cu_seqlens=t, block_table=t, N=256, Hq=4, Hkv=1,
+                num_pages=8, mask_kind=attn.ATTN_MASK_PAGED_DECODE)
+    for ps in (8, 48, 256):
+        assert _call(page_size=ps, **base) == attn.ATTN_ERR_UNSUPPORTED
+    for ps in (16, 32, 64, 128):  # valid sizes get as far as the missing workspace
+        assert _call(page_size=ps, **base) == attn.ATTN_ERR_WORKSPACE
+    # the split-KV scratch does not depend on the page size
+    sizes = {attn.attn_workspace_bytes(32, 32, 8, 16384, 128, 4, ps) for ps in (16, 32, 64, 128)}
+    assert len(sizes) == 1
+
+
 def test_workspace_bytes():
     assert attn.attn_workspace_bytes(4, 16, 16, 2048, 128, CAUSAL, 0) == 0
     n = attn.attn_workspace_bytes(32, 32, 8, 16384, 128, 4, 64)
@@ -234,6 +283,24 @@ def test_units_dense_order_and_cover(kind):
     assert sorted(u) == sorted(itertools.product(range(B), range(Hq), range(npairs)))
     levels = [t for _, _, t in u]
     assert levels == sorted(levels, reverse=True)
+
+
+def test_units_paged_prefill_order_and_cover():
+    """Chunk units: every (sequence, head, pair of the chunk) once, ordered by pair index plus
+    the pairs of context before the chunk, descending."""
+    lq = np.array([1, 300, 0, 2048, 700])
+    lk = np.array([5000, 300, 10, 2100, 16384])
+    cu = np.concatenate([[0], np.cumsum(lq)]).astype(np.int32)
+    Hq = 2
+    u = attn.attn_plan_units(attn.ATTN_MASK_PAGED_PREFILL, len(lq), Hq, int(cu[-1]), cu, lk)
+    want = [(s, h, t) for s in range(len(lq)) for h in range(Hq)
+            for t in range((int(lq[s]) + 255) // 256)]
+    assert sorted(u) == sorted(want)
+    levels = [t + (int(lk[s]) - int(lq[s])) // 256 for s, _, t in u]
+    assert levels == sorted(levels, reverse=True)
+    bad = np.array([0, 5, 10], dtype=np.int32)  # second chunk longer than its context
+    with pytest.raises(attn.AttnError):
+        attn.attn_plan_units(attn.ATTN_MASK_PAGED_PREFILL, 2, 1, 10, bad, np.array([5, 4]))
 
 
 @pytest.mark.parametrize("kind", [DOCUMENT, DOCUMENT_BIDIR])

@@ -204,6 +204,113 @@ def test_dense_decode_ragged(d, group):
     compare(w, run(w), strict=False)
 
 
+@pytest.mark.parametrize("page_size", [16, 32, 128])
+@pytest.mark.parametrize("d", [64, 128])
+def test_paged_decode_page_sizes(d, page_size):
+    lens = [1, 15, 16, 17, 63, 64, 65, 127, 128, 129, 1000, 3000]
+    w = I.paged_decode_workload(450 + page_size, len(lens), 0, 0, 8, 2, d,
+                                page_size=page_size, context_lens=lens)
+    compare(w, run(w), strict=False)
+
+
+def test_paged_decode_page_size_invariant_bit_exact():
+    """The same tokens in pools of 16-, 32-, 64- and 128-token pages fill the decode's
+    64-token stages identically, so the results agree bit for bit."""
+    lens = [1, 100, 2000, 777]
+    outs = []
+    for ps in (16, 32, 64, 128):
+        w = I.paged_decode_workload(46, len(lens), 0, 0, 16, 4, 128, page_size=ps,
+                                    context_lens=lens)
+        dp = run(w)
+        outs.append((dp.o.view(torch.int16).clone(), dp.lse.clone()))
+    for o, l in outs[1:]:
+        assert torch.equal(o, outs[0][0]) and torch.equal(l, outs[0][1])
+
+
+# ------------------------------------------------------------------ chunked prefill, paged KV
+
+@pytest.mark.parametrize("page_size", [16, 32, 64, 128])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("group", [1, 4])
+def test_paged_prefill_ragged(d, page_size, group):
+    """Contexts and chunks of ragged lengths (chunk = whole context, single tokens, chunks
+    crossing tile and page edges); pool tails and spare pages hold poison."""
+    lk = [1, 40, 300, 1000, 2100, 129, 777]
+    lq = [1, 40, 129, 1, 700, 128, 300]
+    w = I.paged_prefill_workload(900 + page_size + group, len(lk), 0, 0, 0, 0, 2 * group, 2, d,
+                                 page_size=page_size, context_lens=lk, chunk_lens=lq)
+    compare(w, run(w), strict=False)
+
+
+def test_paged_prefill_whole_context_equals_document_bit_exact():
+    """A chunk that is the whole context runs the same tiles and masks as the causal document
+    kernel on the gathered tokens."""
+    lens = [300, 129, 700, 1]
+    w = I.paged_prefill_workload(47, len(lens), 0, 0, 0, 0, 8, 2, 128, page_size=16,
+                                 context_lens=lens, chunk_lens=lens)
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    dw = I.document_workload(0, int(cu[-1]), 8, 128, cu_seqlens=cu, Hkv=2)
+    dw.q[...] = w.q
+    for b, L in enumerate(lens):
+        pages = [int(w.block_table[b, p]) for p in range((L + 15) // 16)]
+        dw.k[0, :, cu[b]:cu[b + 1]] = np.concatenate([w.k[p] for p in pages], axis=1)[:, :L]
+        dw.v[0, :, cu[b]:cu[b + 1]] = np.concatenate([w.v[p] for p in pages], axis=1)[:, :L]
+    a, b = run(w), run(dw)
+    assert torch.equal(a.o.view(torch.int16), b.o.view(torch.int16))
+    assert torch.equal(a.lse, b.lse)
+
+
+def test_paged_prefill_page_size_invariant_bit_exact():
+    lk, lq = [1000, 50, 3000], [333, 50, 1]
+    outs = []
+    for ps in (16, 64, 128):
+        w = I.paged_prefill_workload(48, 3, 0, 0, 0, 0, 8, 2, 128, page_size=ps,
+                                     context_lens=lk, chunk_lens=lq)
+        dp = run(w)
+        outs.append((dp.o.view(torch.int16).clone(), dp.lse.clone()))
+    for o, l in outs[1:]:
+        assert torch.equal(o, outs[0][0]) and torch.equal(l, outs[0][1])
+
+
+@pytest.mark.parametrize("cfg", ["6", "6p64"])
+def test_chunked_prefill_workload_sampled(cfg):
+    """Full-size chunked prefill in the launch configuration the benchmark suite times:
+    sampled rows (each chunk's first and last rows, and random rows)."""
+    w = I.config(cfg)
+    dp = run(w)
+    rng = np.random.default_rng(9)
+    n = int(np.prod(w.lse_shape))
+    firsts = w.cu_seqlens[:-1].astype(np.int64)
+    lasts = w.cu_seqlens[1:].astype(np.int64) - 1
+    heads = np.arange(w.Hq)[:, None] * w.N
+    rows = np.unique(np.concatenate([rng.integers(0, n, 1500), (heads + firsts).ravel(),
+                                     (heads + lasts).ravel()]))
+    compare(w, dp, rows=rows)
+
+
+def test_paged_prefill_bad_table_entry_reports_bounds():
+    w = I.paged_prefill_workload(49, 2, 0, 0, 0, 0, 4, 2, 128, page_size=16,
+                                 context_lens=[200, 100], chunk_lens=[50, 100])
+    w.block_table[1, 2] = w.k.shape[0] + 7
+    dp = DeviceProblem(w)
+    assert dp.run() == 0
+    torch.cuda.synchronize()
+    assert attn.attn_get_status() == attn.ATTN_ERR_BOUNDS
+    # sequence 0 is unaffected
+    rows = (np.arange(w.Hq)[:, None] * w.N + np.arange(50)[None, :]).ravel()
+    compare(w, dp, rows=rows)
+
+
+def test_paged_prefill_chunk_longer_than_context_reports_status():
+    w = I.paged_prefill_workload(50, 2, 0, 0, 0, 0, 4, 2, 64, page_size=16,
+                                 context_lens=[64, 100], chunk_lens=[64, 100])
+    w.seqlens_k = np.array([64, 90], dtype=np.int32)  # chunk 100 > context 90
+    dp = DeviceProblem(w)
+    assert dp.run() == 0
+    torch.cuda.synchronize()
+    assert attn.attn_get_status() == attn.ATTN_ERR_SEQLENS
+
+
 def test_dense_decode_empty_context():
     w = I.dense_decode_workload(9, 3, 0, 0, 8, 2, 128, N=100, context_lens=[0, 70, 0])
     dp = run(w)

@@ -23,6 +23,7 @@ ATTN_MASK_DECODE = 5
 ATTN_MASK_SLIDING_BIDIR = 6
 ATTN_MASK_DOCUMENT_BIDIR = 7
 ATTN_MASK_PREFIX_LM = 8
+ATTN_MASK_PAGED_PREFILL = 9
 
 ATTN_OK = 0
 ATTN_ERR_INVALID = -1
@@ -40,6 +41,8 @@ _i = ctypes.c_int
 _SIGS = {
     "attn_fwd": (_i, [_p, _p, _p, _p, _p, _i, _i, _i, _i, _i, ctypes.c_float, _i, _i, _p, _p, _i,
                       _i, _p, ctypes.c_size_t, _p]),
+    "attn_fwd_paged_prefill": (_i, [_p, _p, _p, _p, _p, _i, _i, _i, _i, _i, ctypes.c_float, _p,
+                                    _p, _p, _i, _i, _i, _p]),
     "attn_workspace_bytes": (ctypes.c_size_t, [_i, _i, _i, _i, _i, _i, _i]),
     "attn_gather_pages": (_i, [_p, _p, _p, _i, _i, _i, _i, _i, _i, _p]),
     "attn_get_status": (_i, [_p]),
@@ -118,6 +121,16 @@ def attn_fwd(q, k, v, o, lse, B, Hq, Hkv, N, d, scale, mask_kind, window=0, cu_s
                           _stream(stream))
 
 
+def attn_fwd_paged_prefill(q, k, v, o, lse, B, Hq, Hkv, total_q, d, scale, cu_seqlens_q,
+                           seqlens_k, block_table, max_pages, page_size, num_pages,
+                           stream=None) -> int:
+    """Chunked prefill over a paged KV cache (torch tensors in device memory)."""
+    return lib().attn_fwd_paged_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq,
+                                        Hkv, total_q, d, ctypes.c_float(scale),
+                                        _ptr(cu_seqlens_q), _ptr(seqlens_k), _ptr(block_table),
+                                        max_pages, page_size, num_pages, _stream(stream))
+
+
 def attn_paged_decode_noalloc(q, k, v, o, lse, B, Hq, Hkv, N, d, scale, cu_seqlens, block_table,
                               page_size, num_pages, stream=None) -> int:
     """Paged decode without a workspace argument (the library's fixed scratch is used)."""
@@ -166,9 +179,12 @@ def attn_plan_tile_kind(mask_kind, window, r0, bm, row_end, k_org, k_end, bn, t)
     return lib().attn_plan_tile_kind(mask_kind, window, r0, bm, row_end, k_org, k_end, bn, t)
 
 
-def attn_plan_units(mask_kind, B, Hq, N, cu_seqlens=None):
-    """Prefill work list in launch order: list of (batch-or-segment, head, pair) tuples."""
+def attn_plan_units(mask_kind, B, Hq, N, cu_seqlens=None, seqlens_k=None):
+    """Prefill work list in launch order: list of (batch-or-segment, head, pair) tuples.
+    For ATTN_MASK_PAGED_PREFILL pass the chunk starts and the context lengths."""
     import numpy as np
+    if seqlens_k is not None:
+        cu_seqlens = np.concatenate([np.asarray(cu_seqlens), np.asarray(seqlens_k)])
     cu = None if cu_seqlens is None else np.ascontiguousarray(cu_seqlens, dtype=np.int32)
     cu_p = None if cu is None else cu.ctypes.data
     n = lib().attn_plan_units(mask_kind, B, Hq, N, cu_p, None, 0)

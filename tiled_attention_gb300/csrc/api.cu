@@ -126,6 +126,10 @@ bool prefill_kind(int m) {
 
 bool document_kind(int m) { return m == ATTN_MASK_DOCUMENT || m == ATTN_MASK_DOCUMENT_BIDIR; }
 
+// Page sizes of the paged kinds: multiples of the 8-row swizzle atom that divide the
+// 128-row prefill tile and either divide or are twice the 64-row decode stage.
+bool page_size_ok(int p) { return p == 16 || p == 32 || p == 64 || p == 128; }
+
 // The window argument: SLIDING needs >= 1 key, SLIDING_BIDIR >= 0 keys per side, PREFIX_LM a
 // prefix of >= 0 tokens; the other kinds ignore it.
 bool window_ok(int m, int window) {
@@ -135,8 +139,8 @@ bool window_ok(int m, int window) {
 }
 
 constexpr unsigned long long kTimeoutNs = 2000000000ull;  // 2 s per pipeline wait
-constexpr int kDecodeChunkPages = 16;
-constexpr int kDecodePage = 64;  // tokens per page (the pool's, or 64-row slices of a cache)
+constexpr int kDecodeChunkPages = 16;  // 64-token stages per split
+constexpr int kDecodeStage = 64;       // tokens per decode ring stage
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct DecodeLayout {
@@ -146,9 +150,10 @@ struct DecodeLayout {
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
-DecodeLayout decode_layout(int B, int Hq, int Hkv, int N, int d, int page_size) {
+// Split-KV scratch: splits of kDecodeChunkPages 64-token stages over contexts of up to N.
+DecodeLayout decode_layout(int B, int Hq, int Hkv, int N, int d) {
   DecodeLayout L{};
-  L.max_pages = (N + page_size - 1) / page_size;
+  L.max_pages = (N + kDecodeStage - 1) / kDecodeStage;
   L.max_splits = (L.max_pages + kDecodeChunkPages - 1) / kDecodeChunkPages;
   const size_t groups = static_cast<size_t>(B) * Hkv;
   const size_t G = Hkv > 0 ? static_cast<size_t>(Hq / Hkv) : 0;
@@ -234,11 +239,11 @@ const char* attn_last_error(void) { return g_last_error.c_str(); }
 
 size_t attn_workspace_bytes(int B, int Hq, int Hkv, int N, int d, int mask_kind,
                             int page_size) {
-  if (mask_kind == ATTN_MASK_DECODE) page_size = kDecodePage;
+  if (mask_kind == ATTN_MASK_DECODE) page_size = kDecodeStage;
   if ((mask_kind != ATTN_MASK_PAGED_DECODE && mask_kind != ATTN_MASK_DECODE) || B <= 0 ||
       Hkv <= 0 || Hq <= 0 || N <= 0 || page_size <= 0 || d <= 0)
     return 0;
-  return decode_layout(B, Hq, Hkv, N, d, page_size).total;
+  return decode_layout(B, Hq, Hkv, N, d).total;
 }
 
 int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
@@ -269,8 +274,8 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
   if (decode) {
     if (mask_kind == ATTN_MASK_PAGED_DECODE) {
       if (!block_table) return fail(ATTN_ERR_INVALID, "block_table is required");
-      if (page_size != kDecodePage)
-        return fail(ATTN_ERR_UNSUPPORTED, "page_size %d (%d)", page_size, kDecodePage);
+      if (!page_size_ok(page_size))
+        return fail(ATTN_ERR_UNSUPPORTED, "page_size %d (16, 32, 64 or 128)", page_size);
       if (num_pages <= 0) return fail(ATTN_ERR_INVALID, "num_pages %d", num_pages);
       if (static_cast<long long>(num_pages) * Hkv >= (1ll << 31))
         return fail(ATTN_ERR_UNSUPPORTED, "page pool too large");
@@ -279,7 +284,7 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
     }
     if (group != 1 && group != 2 && group != 4 && group != 8 && group != 16)
       return fail(ATTN_ERR_UNSUPPORTED, "query heads per kv head %d (1, 2, 4, 8, 16)", group);
-    L = decode_layout(B, Hq, Hkv, N, d, kDecodePage);
+    L = decode_layout(B, Hq, Hkv, N, d);
     if (L.max_splits > 65535 || Hkv > 65535 || B > 65535)
       return fail(ATTN_ERR_UNSUPPORTED, "decode grid too large");
     if (!workspace || workspace_bytes < L.total || !aligned16(workspace))
@@ -297,15 +302,16 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
   if (rc) return rc;
 
   if (decode) {
-    // PAGED_DECODE: the pools as [num_pages * Hkv][64][d]; DECODE: the dense caches as
-    // [B * Hkv][N][d]. Boxes of 64 rows: one page of one kv head.
+    // PAGED_DECODE: the pools as [num_pages * Hkv][page_size][d], boxes of min(page_size, 64)
+    // rows; DECODE: the dense caches as [B * Hkv][N][d], boxes of 64 rows.
     const bool dense = mask_kind == ATTN_MASK_DECODE;
-    const uint64_t rows = dense ? static_cast<uint64_t>(N) : kDecodePage;
+    const uint64_t rows = dense ? static_cast<uint64_t>(N) : static_cast<uint64_t>(page_size);
     const uint64_t planes = dense ? static_cast<uint64_t>(B) * Hkv
                                   : static_cast<uint64_t>(num_pages) * Hkv;
+    const uint32_t box = dense ? kDecodeStage : static_cast<uint32_t>(imin(page_size, kDecodeStage));
     CUtensorMap tk, tv;
-    if ((rc = encode_3d(&tk, k, d, rows, planes, kDecodePage))) return rc;
-    if ((rc = encode_3d(&tv, v, d, rows, planes, kDecodePage))) return rc;
+    if ((rc = encode_3d(&tk, k, d, rows, planes, box))) return rc;
+    if ((rc = encode_3d(&tv, v, d, rows, planes, box))) return rc;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     DecodeParams p{};
     p.q = static_cast<const uint4*>(q);
@@ -320,9 +326,10 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
     p.B = B;
     p.Hq = Hq;
     p.Hkv = Hkv;
-    p.max_pages = L.max_pages;
+    p.max_pages = dense ? 0 : (N + page_size - 1) / page_size;
     p.num_pages = dense ? 0 : num_pages;
-    p.max_len = dense ? N : L.max_pages * kDecodePage;
+    p.page_size = dense ? kDecodeStage : page_size;
+    p.max_len = N;
     p.max_splits = L.max_splits;
     p.chunk_pages = kDecodeChunkPages;
     p.scale_log2 = scale * kLog2e;
@@ -369,6 +376,72 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
   cudaError_t e = d == 64 ? launch_prefill_d64(mask_kind, tq, tk, tv, to, p, grid, stream)
                           : launch_prefill_d128(mask_kind, tq, tk, tv, to, p, grid, stream);
   if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
+  return ATTN_OK;
+}
+
+int attn_fwd_paged_prefill(const void* q, const void* k, const void* v, void* o, float* lse,
+                           int B, int Hq, int Hkv, int total_q, int d, float scale,
+                           const int32_t* cu_seqlens_q, const int32_t* seqlens_k,
+                           const int32_t* block_table, int max_pages, int page_size,
+                           int num_pages, void* stream) {
+  g_last_error.clear();
+  if (B < 0 || total_q < 0 || Hq <= 0 || Hkv <= 0)
+    return fail(ATTN_ERR_INVALID, "need B >= 0, total_q >= 0, Hq > 0, Hkv > 0");
+  if (Hq % Hkv != 0) return fail(ATTN_ERR_INVALID, "Hq (%d) %% Hkv (%d) != 0", Hq, Hkv);
+  if (d != 64 && d != 128) return fail(ATTN_ERR_UNSUPPORTED, "head dim %d (64 or 128)", d);
+  if (!std::isfinite(scale)) return fail(ATTN_ERR_INVALID, "scale is not finite");
+  if (!(scale > 0.f)) return fail(ATTN_ERR_UNSUPPORTED, "scale must be > 0");
+  if (!page_size_ok(page_size))
+    return fail(ATTN_ERR_UNSUPPORTED, "page_size %d (16, 32, 64 or 128)", page_size);
+  if (B == 0 || total_q == 0) return ATTN_OK;  // no query rows
+  if (!q || !k || !v || !o || !lse || !cu_seqlens_q || !seqlens_k || !block_table)
+    return fail(ATTN_ERR_INVALID, "null pointer");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return fail(ATTN_ERR_INVALID, "tensors must be 16-byte aligned");
+  if (max_pages <= 0 || num_pages <= 0)
+    return fail(ATTN_ERR_INVALID, "max_pages %d, num_pages %d", max_pages, num_pages);
+  if (static_cast<long long>(num_pages) * Hkv >= (1ll << 31) ||
+      static_cast<long long>(max_pages) * page_size >= (1ll << 31))
+    return fail(ATTN_ERR_UNSUPPORTED, "page pool or block table too large");
+  const long long units = static_cast<long long>(Hq) * (total_q / kUnitRows + B);
+  if (units >= (1ll << 31) - 1) return fail(ATTN_ERR_UNSUPPORTED, "too many work units");
+  int* status = nullptr;
+  int rc = status_ptr(&status);
+  if (rc) return rc;
+  // Q, O, LSE packed [1, Hq, total_q]; the pools as [num_pages * Hkv][page_size][d] with one
+  // page per box.
+  CUtensorMap tq, tk, tv, to;
+  if ((rc = encode_3d(&tq, q, d, total_q, Hq, 128))) return rc;
+  if ((rc = encode_3d(&to, o, d, total_q, Hq, 32))) return rc;
+  const uint64_t planes = static_cast<uint64_t>(num_pages) * Hkv;
+  if ((rc = encode_3d(&tk, k, d, page_size, planes, page_size))) return rc;
+  if ((rc = encode_3d(&tv, v, d, page_size, planes, page_size))) return rc;
+  PrefillParams p{};
+  p.o = o;
+  p.lse = lse;
+  p.cu_seqlens = cu_seqlens_q;
+  p.seqlens_k = seqlens_k;
+  p.table = block_table;
+  p.max_pages = max_pages;
+  p.page_size = page_size;
+  p.num_pages = num_pages;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.N = total_q;
+  p.group = Hq / Hkv;
+  p.num_units = static_cast<int>(units);
+  p.window = 0;
+  p.scale_log2 = scale * kLog2e;
+  p.status = status;
+  p.timeout_ns = kTimeoutNs;
+  int sms = 0;
+  if ((rc = sm_count(&sms))) return rc;
+  const int grid = p.num_units < sms ? p.num_units : sms;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = d == 64 ? launch_prefill_d64(kMaskPagedPrefill, tq, tk, tv, to, p, grid, st)
+                          : launch_prefill_d128(kMaskPagedPrefill, tq, tk, tv, to, p, grid, st);
+  if (e != cudaSuccess) return cuda_fail(e, "paged prefill launch");
   return ATTN_OK;
 }
 
@@ -442,9 +515,28 @@ int attn_plan_tile_kind(int mask_kind, int window, int r0, int bm, int row_end, 
 
 int attn_plan_units(int mask_kind, int B, int Hq, int N, const int32_t* cu, int32_t* out,
                     int max_units) {
-  if (B < 0 || Hq <= 0 || N < 0 || !prefill_kind(mask_kind)) return ATTN_ERR_INVALID;
+  const bool paged = mask_kind == ATTN_MASK_PAGED_PREFILL;
+  if (B < 0 || Hq <= 0 || N < 0 || !(prefill_kind(mask_kind) || paged))
+    return ATTN_ERR_INVALID;
   std::vector<int32_t> units;
-  if (!document_kind(mask_kind)) {
+  if (paged) {
+    // cu holds the chunk starts [B+1] followed by the context lengths [B]. A unit's level is
+    // its pair index plus the pairs of context before its chunk.
+    if (!cu) return ATTN_ERR_INVALID;
+    const int32_t* lk = cu + B + 1;
+    int tmax = 0;
+    for (int s = 0; s < B; ++s) {
+      const int len = cu[s + 1] - cu[s];
+      if (len < 0 || lk[s] < len) return ATTN_ERR_SEQLENS;
+      tmax = imax(tmax, (lk[s] - len) / kUnitRows + pairs_for_rows(len));
+    }
+    for (int t = tmax - 1; t >= 0; --t)
+      for (int s = 0; s < B; ++s) {
+        const int l0 = (lk[s] - (cu[s + 1] - cu[s])) / kUnitRows;
+        if (t >= l0 && t < l0 + pairs_for_rows(cu[s + 1] - cu[s]))
+          for (int h = 0; h < Hq; ++h) units.insert(units.end(), {s, h, t - l0});
+      }
+  } else if (!document_kind(mask_kind)) {
     const int npairs = pairs_for_rows(N);
     for (int level = npairs - 1; level >= 0; --level)
       for (int b = 0; b < B; ++b)

@@ -1,15 +1,16 @@
 // decode.cuh — paged-KV decode (one query token per sequence) with split-KV partials and a
 // fused log-sum-exp-weighted combine.
 //
-// The KV cache is a pool of pages [num_pages, Hkv, 64, D]; sequence b's logical page p lives
-// at physical page block_table[b][p] ("Optimizing Triton Kernels for Custom Attention
-// Patterns on H100", Pattern C). Instead of first gathering pages into a dense buffer, the
-// producer warp issues one TMA box per (page, kv-head, 64 columns) straight from the pool into
-// a shared-memory ring, so every K/V byte crosses HBM once. The same kernel also reads dense
+// The KV cache is a pool of pages [num_pages, Hkv, P, D] (P = 16, 32, 64 or 128 tokens);
+// sequence b's logical page p lives at physical page block_table[b][p] ("Optimizing Triton
+// Kernels for Custom Attention Patterns on H100", Pattern C). Instead of first gathering pages
+// into a dense buffer, the producer warp issues TMA boxes straight from the pool into a
+// shared-memory ring of 64-token stages (64/P pages per stage, or half a 128-token page), so
+// every K/V byte crosses HBM once. The same kernel also reads dense
 // per-sequence caches [B, Hkv, L, D] (p.dense): the second stage of that page's two-stage
 // path, which first gathers the pages into such a cache.
 //
-// Grid (split, kv head g, sequence b): a CTA handles `chunk_pages` pages of one (b, g) for
+// Grid (split, kv head g, sequence b): a CTA handles `chunk_pages` 64-token stages of one (b, g) for
 // all G = Hq/Hkv query heads of the group. Decode reads each K/V byte once and is HBM-bound;
 // the arithmetic only has to stay off the critical path. It runs as warp-level bf16 MMAs
 // (mma.sync m16n8k16, fp32 accumulate) with the G heads as the rows of a 16-row tile: an
@@ -36,15 +37,16 @@ namespace ta {
 struct DecodeParams {
   const uint4* q;        // bf16 [B, Hq, 1, D]
   const int* cu;         // [B+1] cumulative context lengths
-  const int* table;      // [B, max_pages]
+  const int* table;      // [B, max_pages] (max_pages = ceil(longest context / page_size))
   void* o;               // bf16 [B, Hq, 1, D]
   float* lse;            // [B, Hq]
   float* part_o;         // [B*Hkv, max_splits, G, D]
   float* part_ml;        // [B*Hkv, max_splits, G, 2]
   int* counters;         // [B*Hkv], zero before the launch
   int B, Hq, Hkv, max_pages, num_pages, max_splits, chunk_pages;
+  int page_size;         // tokens per pool page (paged); a TMA box holds min(page_size, 64)
   int dense;             // 1: K/V are dense caches [B*Hkv, max_len, D], no block table
-  int max_len;           // longest valid context (dense: the cache rows; paged: table span)
+  int max_len;           // longest valid context (N: the cache rows, or the table's reach)
   float scale_log2;
   int* status;
   unsigned long long timeout_ns;
@@ -52,7 +54,7 @@ struct DecodeParams {
 
 template <int D, int G>
 struct DecodeCfg {
-  static constexpr int kPage = 64;
+  static constexpr int kPage = 64;  // tokens per ring stage
   static constexpr int kWarps = 4;  // consumer warp w owns tokens [16w, 16w + 16) of each page
   static constexpr int kConsumers = kWarps * 32;
   static constexpr int kThreads = kConsumers + 32;
@@ -172,7 +174,39 @@ __global__ void __launch_bounds__(160, 2)
     if (lane == 0) {
       prefetch_tensormap(&tm_k);
       prefetch_tensormap(&tm_v);
-      const int* row = p.dense ? nullptr : p.table + static_cast<size_t>(b) * p.max_pages + pg0;
+      const int* row = p.dense ? nullptr : p.table + static_cast<size_t>(b) * p.max_pages;
+      // Paged: stage k holds tokens 64 (pg0 + k) .. + 63 in boxes of `rows` tokens. The boxes'
+      // planes and first rows are looked up one stage ahead (table reads issued together), so
+      // their latency hides behind the current stage. A box whose first token is past the
+      // context, or whose table entry is outside the pool (never addressed; the status word
+      // reports it), is loaded from the plane just past the pool, which TMA fills with zeros,
+      // so the stage always receives its full bytes.
+      const int P = p.dense ? C::kPage : p.page_size;
+      const int rows = P < C::kPage ? P : C::kPage;
+      int pl[4], r0[4], pl_next[4], r0_next[4];
+      auto stage_boxes = [&](int k, int (&pl_o)[4], int (&r0_o)[4]) {
+        int raw[4];
+#pragma unroll
+        for (int sb = 0; sb < 4; ++sb) {
+          const int tok = (pg0 + k) * C::kPage + sb * rows;
+          raw[sb] = (sb < C::kPage / rows && tok < L) ? __ldg(row + tok / P) : -1;
+        }
+#pragma unroll
+        for (int sb = 0; sb < 4; ++sb) {
+          const int tok = (pg0 + k) * C::kPage + sb * rows;
+          pl_o[sb] = p.num_pages * p.Hkv;
+          r0_o[sb] = 0;
+          if (sb < C::kPage / rows && tok < L) {
+            if (raw[sb] < 0 || raw[sb] >= p.num_pages) {
+              report_status(p.status, -5);
+            } else {
+              pl_o[sb] = raw[sb] * p.Hkv + g;
+              r0_o[sb] = tok % P;
+            }
+          }
+        }
+      };
+      if (!p.dense && n > 0) stage_boxes(0, pl_next, r0_next);
       int issued = 0;
       for (int k = 0; k < n; ++k) {
         const int st = k % S;
@@ -193,22 +227,24 @@ __global__ void __launch_bounds__(160, 2)
           }
           continue;
         }
-        const int phys = row[k];
-        if (phys < 0 || phys >= p.num_pages) {
-          // Out-of-pool entry: never address it. The stage completes without data and the
-          // status word tells the caller the result is invalid.
-          report_status(p.status, -5);
-          mbar_arrive(&ctl->full[st]);
-          continue;
+#pragma unroll
+        for (int sb = 0; sb < 4; ++sb) {
+          pl[sb] = pl_next[sb];
+          r0[sb] = r0_next[sb];
         }
         mbar_arrive_expect_tx(&ctl->full[st], C::kStageBytes);
-        const int plane = phys * p.Hkv + g;
 #pragma unroll
-        for (int pn = 0; pn < C::kPanels; ++pn) {
-          tma_load_3d(dst + pn * C::kPanelBytes, &tm_k, &ctl->full[st], pn * 64, 0, plane);
-          tma_load_3d(dst + C::kPageBytes + pn * C::kPanelBytes, &tm_v, &ctl->full[st], pn * 64,
-                      0, plane);
+        for (int sb = 0; sb < 4; ++sb) {
+          if (sb >= C::kPage / rows) break;
+#pragma unroll
+          for (int pn = 0; pn < C::kPanels; ++pn) {
+            tma_load_3d(dst + pn * C::kPanelBytes + sb * rows * 128, &tm_k, &ctl->full[st],
+                        pn * 64, r0[sb], pl[sb]);
+            tma_load_3d(dst + C::kPageBytes + pn * C::kPanelBytes + sb * rows * 128, &tm_v,
+                        &ctl->full[st], pn * 64, r0[sb], pl[sb]);
+          }
         }
+        if (k + 1 < n) stage_boxes(k + 1, pl_next, r0_next);
       }
       for (int k = imax(0, issued - S); k < issued; ++k)
         mbar_wait(&ctl->full[k % S], (k / S) & 1, wc_drain);

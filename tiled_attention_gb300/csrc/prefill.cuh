@@ -1,5 +1,6 @@
 // prefill.cuh — fused tiled attention forward for sm_103a (no mask, causal, sliding window
-// one- and two-sided, document segments causal and non-causal, prefix-LM).
+// one- and two-sided, document segments causal and non-causal, prefix-LM, and chunked prefill
+// over a paged KV cache).
 //
 // Work unit: two 128-row query tiles of one (batch or segment, query head). The kernel is
 // persistent, one CTA per SM: CTA b of G takes units b, 2G-1-b, 2G+b, 4G-1-b, ... of the
@@ -44,7 +45,10 @@ namespace ta {
 struct PrefillParams {
   void* o;                  // bf16 [planes, N, D]
   float* lse;               // fp32 [planes, N]
-  const int* cu_seqlens;    // DOCUMENT: [B+1]
+  const int* cu_seqlens;    // packed kinds: [B+1] segment / query-chunk starts
+  const int* seqlens_k;     // PAGED_PREFILL: [B] context lengths (each chunk included)
+  const int* table;         // PAGED_PREFILL: [B, max_pages] block table
+  int max_pages, page_size, num_pages;  // PAGED_PREFILL
   int B, Hq, Hkv, N, group; // N: rows per (batch, head) plane (T for DOCUMENT)
   int num_units;            // work units; DOCUMENT: an upper bound (surplus ones decode invalid)
   int window;               // SLIDING / SLIDING_BIDIR window, PREFIX_LM prefix length
@@ -94,16 +98,30 @@ struct PrefillCtrl {
 };
 
 struct Unit {
-  int valid, bh, kvh, q_row0, k_org, k_end;
+  int valid, bh, kvh, q_row0, k_org, k_end, seq;
 };
 
-// Work unit u in launch order: pair levels from the deepest (most key tiles) down, then
-// batch / segment, then head (heads sharing a kv head are adjacent).
+// Position of one role in the packed unit list. Every role of a CTA visits its units in
+// increasing order (round k takes unit kG + b or kG + G-1-b), so each keeps a cursor: the level
+// it stands on, the number of units on the levels above it, and the number of segments on it.
+// A unit then costs one scan over the segments, plus one more per level passed.
+struct UnitCursor {
+  int started;  // the segment lengths have been checked and tmax found
+  int t;        // current level (tmax before the first one)
+  int base;     // units on the levels above t
+  int cnt;      // segments holding level t (0 before the first level)
+};
+
+// Work unit u in launch order: levels from the deepest (most key tiles) down, then batch /
+// segment, then head (heads sharing a kv head are adjacent). The level of a unit is its pair
+// index inside its segment, plus, for PAGED_PREFILL, the pairs of context that precede the
+// chunk ((context - chunk) / 256), so long contexts start first. Units must be asked for in
+// increasing order with the same cursor; warp-collective.
 template <int MASK>
-__device__ __forceinline__ Unit decode_unit(int u, const PrefillParams& p) {
-  Unit r{0, 0, 0, 0, 0, 0};
+__device__ __forceinline__ Unit decode_unit(int u, const PrefillParams& p, UnitCursor& cur) {
+  Unit r{0, 0, 0, 0, 0, 0, 0};
   const int lane = static_cast<int>(lane_id());
-  if (!is_document(MASK)) {
+  if (!is_packed(MASK)) {
     const int per_level = p.B * p.Hq;
     const int npairs = pairs_for_rows(p.N);
     if (u >= per_level * npairs) return r;
@@ -117,57 +135,91 @@ __device__ __forceinline__ Unit decode_unit(int u, const PrefillParams& p) {
     r.k_end = p.N;
     return r;
   }
-  // DOCUMENT: the warp scans the segments 32 at a time.
+  // Packed kinds: the warp scans the segments 32 at a time.
   const int* cu = p.cu_seqlens;
-  int tmax = 0;
-  bool bad = false;
-  for (int s0 = 0; s0 < p.B; s0 += 32) {
-    const int s = s0 + lane;
-    if (s < p.B) {
-      const int len = cu[s + 1] - cu[s];
-      bad |= len < 0;
-      tmax = imax(tmax, pairs_for_rows(imax(len, 0)));
-    }
-  }
-  for (int off = 16; off; off >>= 1) tmax = imax(tmax, __shfl_xor_sync(0xffffffffu, tmax, off));
-  bad = __any_sync(0xffffffffu, bad) || cu[0] != 0 || cu[p.B] != p.N;
-  if (bad) {
-    if (u == 0 && lane == 0) report_status(p.status, -7);
-    return r;
-  }
-  int rem = u;
-  for (int t = tmax - 1; t >= 0; --t) {
-    int cnt = 0;
+  // First level of segment s.
+  auto level0 = [&](int s) {
+    return MASK == kMaskPagedPrefill ? (p.seqlens_k[s] - (cu[s + 1] - cu[s])) / kUnitRows : 0;
+  };
+  if (!cur.started) {
+    int tmax = 0;
+    bool bad = false;
     for (int s0 = 0; s0 < p.B; s0 += 32) {
       const int s = s0 + lane;
-      const bool has = s < p.B && pairs_for_rows(cu[s + 1] - cu[s]) > t;
-      cnt += __popc(__ballot_sync(0xffffffffu, has));
-    }
-    if (rem < cnt * p.Hq) {
-      const int idx = rem / p.Hq;
-      const int h = rem % p.Hq;
-      int seen = 0, seg = -1;
-      for (int s0 = 0; s0 < p.B && seg < 0; s0 += 32) {
-        const int s = s0 + lane;
-        const bool has = s < p.B && pairs_for_rows(cu[s + 1] - cu[s]) > t;
-        unsigned m = __ballot_sync(0xffffffffu, has);
-        const int c = __popc(m);
-        if (idx < seen + c) {
-          for (int z = 0; z < idx - seen; ++z) m &= m - 1;
-          seg = s0 + __ffs(m) - 1;
+      if (s < p.B) {
+        const int len = cu[s + 1] - cu[s];
+        bad |= len < 0;
+        if (MASK == kMaskPagedPrefill) {
+          const int lk = p.seqlens_k[s];
+          bad |= lk < len || lk > p.max_pages * p.page_size;
         }
-        seen += c;
+        if (!bad) tmax = imax(tmax, level0(s) + pairs_for_rows(len));
       }
-      r.valid = 1;
-      r.bh = h;
-      r.kvh = h / p.group;
-      r.k_org = cu[seg];
-      r.k_end = cu[seg + 1];
-      r.q_row0 = r.k_org + t * kUnitRows;
-      return r;
     }
-    rem -= cnt * p.Hq;
+    for (int off = 16; off; off >>= 1)
+      tmax = imax(tmax, __shfl_xor_sync(0xffffffffu, tmax, off));
+    bad = __any_sync(0xffffffffu, bad) || cu[0] != 0 || cu[p.B] != p.N;
+    if (bad) {
+      if (u == 0 && lane == 0) report_status(p.status, -7);
+      cur.t = -1;  // no level: every unit decodes invalid
+    } else {
+      cur.t = tmax;
+    }
+    cur.started = 1;
+    cur.base = 0;
+    cur.cnt = 0;
   }
+  // Segment s has a unit at level t iff level0(s) <= t < level0(s) + its pair count.
+  auto has_level = [&](int s, int t) {
+    const int l0 = level0(s);
+    return t >= l0 && t < l0 + pairs_for_rows(cu[s + 1] - cu[s]);
+  };
+  // Step down to the level holding u, visiting only levels some segment has (for
+  // PAGED_PREFILL a long context puts its chunk's units far above level 0).
+  while (u >= cur.base + cur.cnt * p.Hq) {
+    if (cur.t <= 0) return r;
+    int next = -1;  // the highest level below cur.t that some segment has
+    for (int s0 = 0; s0 < p.B; s0 += 32) {
+      const int s = s0 + lane;
+      if (s < p.B) {
+        const int l0 = level0(s);
+        const int c = imin(cur.t - 1, l0 + pairs_for_rows(cu[s + 1] - cu[s]) - 1);
+        if (c >= l0) next = imax(next, c);
+      }
+    }
+    for (int off = 16; off; off >>= 1)
+      next = imax(next, __shfl_xor_sync(0xffffffffu, next, off));
+    cur.base += cur.cnt * p.Hq;
+    cur.cnt = 0;
+    cur.t = next;
+    if (next < 0) return r;
+    for (int s0 = 0; s0 < p.B; s0 += 32) {
+      const int s = s0 + lane;
+      cur.cnt += __popc(__ballot_sync(0xffffffffu, s < p.B && has_level(s, next)));
+    }
+  }
+  const int t = cur.t;
+  const int idx = (u - cur.base) / p.Hq;
+  const int h = (u - cur.base) % p.Hq;
+  int seen = 0, seg = -1;
+  for (int s0 = 0; s0 < p.B && seg < 0; s0 += 32) {
+    const int s = s0 + lane;
+    unsigned m = __ballot_sync(0xffffffffu, s < p.B && has_level(s, t));
+    const int c = __popc(m);
+    if (idx < seen + c) {
+      for (int z = 0; z < idx - seen; ++z) m &= m - 1;
+      seg = s0 + __ffs(m) - 1;
+    }
+    seen += c;
+  }
+  r.valid = 1;
+  r.bh = h;
+  r.kvh = h / p.group;
+  r.seq = seg;
+  r.k_end = cu[seg + 1];
+  r.q_row0 = cu[seg] + (t - level0(seg)) * kUnitRows;
+  r.k_org = MASK == kMaskPagedPrefill ? cu[seg] - (p.seqlens_k[seg] - (cu[seg + 1] - cu[seg]))
+                                      : cu[seg];
   return r;
 }
 
@@ -266,6 +318,7 @@ __global__ void __launch_bounds__(384, 1)
   };
   // Every role walks the same unit sequence; a Q load is counted only for a query tile with
   // work, in tile order, so all roles agree on which buffer (count % QB) holds which tile.
+  UnitCursor cur{0, 0, 0, 0};  // this role's place in the packed unit list
 
   if (warp < 4) {
     regs_decrease<C::kRegsControl>();
@@ -277,7 +330,7 @@ __global__ void __launch_bounds__(384, 1)
       for (int k = 0; ok; ++k) {
         const int u = unit_of(k);
         if (u >= p.num_units) break;
-        const Unit un = decode_unit<MASK>(u, p);  // warp-collective
+        const Unit un = decode_unit<MASK>(u, p, cur);  // warp-collective
         if (!un.valid) break;
         KvRange rng[2];
         int lo, hi;
@@ -294,6 +347,36 @@ __global__ void __launch_bounds__(384, 1)
               tma_load_3d(q_s + qb * C::kQBytes + c * C::kChunkBytes, &tm_q, &ctl->q_full[qb],
                           c * 64, un.q_row0 + i * BM, un.bh);
           }
+          // PAGED_PREFILL: key tile j of the sequence is BN / P pages, each its own box of P
+          // rows. The planes of a tile's pages are looked up once (all table reads issued
+          // together) for its K and V, and the next tile's while this one's boxes go out. A
+          // page past the context, or whose table entry is outside the pool (never addressed;
+          // the status word reports it), is read from the plane just past the pool, which TMA
+          // fills with zeros, so the stage always receives its full bytes.
+          int pl[8], pl_next[8];
+          auto page_planes = [&](int j, int (&out)[8]) {
+            const int P = p.page_size;
+            const int lk = un.k_end - un.k_org;
+            const int* trow = p.table + static_cast<size_t>(un.seq) * p.max_pages;
+            int raw[8];
+#pragma unroll
+            for (int sb = 0; sb < 8; ++sb) {
+              const int tok = j * BN + sb * P;
+              raw[sb] = (sb < BN / P && tok < lk) ? __ldg(trow + tok / P) : -1;
+            }
+#pragma unroll
+            for (int sb = 0; sb < 8; ++sb) {
+              const int tok = j * BN + sb * P;
+              out[sb] = p.num_pages * p.Hkv;
+              if (sb < BN / P && tok < lk) {
+                if (raw[sb] < 0 || raw[sb] >= p.num_pages)
+                  report_status(p.status, -5);
+                else
+                  out[sb] = raw[sb] * p.Hkv + un.kvh;
+              }
+            }
+          };
+          if (MASK == kMaskPagedPrefill && hi > lo) page_planes(lo, pl_next);
           // Ring entry e holds K_{lo + x/2} (x = e - first entry of the unit, even) or V.
           for (int x = 0; x < 2 * (hi - lo) && ok; ++x, ++e) {
             const int st = e % STAGES;
@@ -301,9 +384,26 @@ __global__ void __launch_bounds__(384, 1)
             if (!ok) break;
             mbar_arrive_expect_tx(&ctl->kv_full[st], C::kKVBytes);
             const CUtensorMap* m = (x & 1) ? &tm_v : &tm_k;
-            for (int c = 0; c < C::kPanels; ++c)
-              tma_load_3d(kv_s + st * C::kKVBytes + c * C::kChunkBytes, m, &ctl->kv_full[st],
-                          c * 64, un.k_org + (lo + x / 2) * BN, un.kvh);
+            uint8_t* dst = kv_s + st * C::kKVBytes;
+            if (MASK == kMaskPagedPrefill) {
+              const int P = p.page_size;
+              if (!(x & 1)) {
+#pragma unroll
+                for (int sb = 0; sb < 8; ++sb) pl[sb] = pl_next[sb];
+              }
+#pragma unroll
+              for (int sb = 0; sb < 8; ++sb) {
+                if (sb >= BN / P) break;
+                for (int c = 0; c < C::kPanels; ++c)
+                  tma_load_3d(dst + c * C::kChunkBytes + sb * P * 128, m, &ctl->kv_full[st],
+                              c * 64, 0, pl[sb]);
+              }
+              if (!(x & 1) && lo + x / 2 + 1 < hi) page_planes(lo + x / 2 + 1, pl_next);
+            } else {
+              for (int c = 0; c < C::kPanels; ++c)
+                tma_load_3d(dst + c * C::kChunkBytes, m, &ctl->kv_full[st], c * 64,
+                            un.k_org + (lo + x / 2) * BN, un.kvh);
+            }
           }
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -328,7 +428,7 @@ __global__ void __launch_bounds__(384, 1)
       for (int k = 0; ok; ++k) {
         const int u = unit_of(k);
         if (u >= p.num_units) break;
-        const Unit un = decode_unit<MASK>(u, p);  // warp-collective
+        const Unit un = decode_unit<MASK>(u, p, cur);  // warp-collective
         if (!un.valid) break;
         KvRange rng[2];
         int lo, hi;
@@ -426,7 +526,7 @@ __global__ void __launch_bounds__(384, 1)
     for (int k = 0; ok; ++k) {
       const int u = unit_of(k);
       if (u >= p.num_units) break;
-      const Unit un = decode_unit<MASK>(u, p);  // warp-collective
+      const Unit un = decode_unit<MASK>(u, p, cur);  // warp-collective
       if (!un.valid) break;
       KvRange rng[2];
       int lo_u, hi_u;
@@ -538,7 +638,7 @@ __global__ void __launch_bounds__(384, 1)
       // DOCUMENT warp whose rows run past its segment writes them one thread per row instead,
       // so the next segment's rows stay untouched.
       const int warp_row0 = q_row0 + i * BM + quarter * 32;
-      const bool staged = !is_document(MASK) || warp_row0 + 31 < row_end;
+      const bool staged = !is_packed(MASK) || warp_row0 + 31 < row_end;
       uint8_t* stage = q_s + (qn % QB) * C::kQBytes;
       uint8_t* orow = static_cast<uint8_t*>(p.o) +
                       (static_cast<size_t>(bh) * p.N + static_cast<size_t>(row)) * D * 2;

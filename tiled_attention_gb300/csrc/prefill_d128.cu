@@ -30,6 +30,7 @@ cudaError_t launch_prefill_d128(int mask, const CUtensorMap& q, const CUtensorMa
     case kMaskDocumentBidir:
       return launch_one<kMaskDocumentBidir>(q, k, v, o, p, grid, stream);
     case kMaskPrefixLM: return launch_one<kMaskPrefixLM>(q, k, v, o, p, grid, stream);
+    case kMaskPagedPrefill: return launch_one<kMaskPagedPrefill>(q, k, v, o, p, grid, stream);
     default: return cudaErrorInvalidValue;
   }
 }

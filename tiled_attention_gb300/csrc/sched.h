@@ -23,10 +23,17 @@ namespace ta {
 
 enum MaskKind { kMaskNone = 0, kMaskCausal = 1, kMaskSliding = 2, kMaskDocument = 3,
                 kMaskPaged = 4, kMaskDecode = 5, kMaskSlidingBidir = 6, kMaskDocumentBidir = 7,
-                kMaskPrefixLM = 8 };
+                kMaskPrefixLM = 8, kMaskPagedPrefill = 9 };
 
-// Kinds whose rows are packed segments described by cu_seqlens.
-TA_HD bool is_document(int mask) { return mask == kMaskDocument || mask == kMaskDocumentBidir; }
+// Kinds whose query rows are packed segments described by cu_seqlens. For PAGED_PREFILL a
+// segment is one sequence's query chunk; its keys (the sequence's context, held in a paged
+// pool) are numbered so that key j sits at index k_org + j with k_org = chunk start -
+// (context length - chunk length). The chunk's last row then lines up with the context's
+// last key, and the causal rule j <= i of that shared index space is the chunked-prefill
+// mask: chunk row t sees the context's keys up to position (context - chunk) + t.
+TA_HD bool is_packed(int mask) {
+  return mask == kMaskDocument || mask == kMaskDocumentBidir || mask == kMaskPagedPrefill;
+}
 
 enum TileKind { kTileEmpty = 0, kTileFull = 1, kTileBoundary = 2 };
 

@@ -375,6 +375,17 @@ def config(k) -> Workload:
     if k == "3p":
         return dense_workload(1003, 2, 32, 8, 8192, 128, MASK_PREFIX_LM, window=4096,
                               name="prefix-LM P4096 B2 Hq32 Hkv8 N8192 d128")
+    # Chunked prefill over a paged cache: 16 sequences with contexts U[2048,16384] whose last
+    # U[256,2048] tokens are the new chunk, vLLM-sized pages of 16 tokens (and 64).
+    if k in ("6", "6p64"):
+        ps = 16 if k == "6" else 64
+        return paged_prefill_workload(1006, 16, 2048, 16384, 256, 2048, 32, 8, 128,
+                                      page_size=ps, name=(
+                                          "chunked prefill B16 Lk U[2048,16384] Lq U[256,2048] "
+                                          f"Hq32 Hkv8 d128 page{ps}"))
+    if k == "5p16":
+        return paged_decode_workload(1005, 32, 1024, 16384, 32, 8, 128, page_size=16, name=(
+            "paged decode B32 L U[1024,16384] Hq32 Hkv8 d128 page16"))
     if k == "4b":
         return document_workload(1004, 16384, 16, 64, 256, 4096, mask_kind=MASK_DOCUMENT_BIDIR,
                                  name="non-causal document T16384 H16 d64 seg U[256,4096]")

@@ -9,7 +9,7 @@ import numpy as np
 import torch
 
 from . import attn
-from .inputs import MASK_PAGED_DECODE, Workload
+from .inputs import MASK_PAGED_DECODE, MASK_PAGED_PREFILL, Workload
 
 
 def bf16_tensor(a: np.ndarray, device) -> torch.Tensor:
@@ -33,13 +33,23 @@ class DeviceProblem:
                    torch.from_numpy(np.ascontiguousarray(w.cu_seqlens, np.int32)).to(self.device))
         self.table = (None if w.block_table is None else
                       torch.from_numpy(np.ascontiguousarray(w.block_table, np.int32)).to(self.device))
-        self.num_pages = int(w.k.shape[0]) if w.mask_kind == MASK_PAGED_DECODE else 0
-        nbytes = attn.attn_workspace_bytes(w.B, w.Hq, w.Hkv, w.N, w.d, w.mask_kind, w.page_size)
+        self.num_pages = (int(w.k.shape[0]) if w.mask_kind in (MASK_PAGED_DECODE,
+                                                                 MASK_PAGED_PREFILL) else 0)
+        self.seqlens_k = (None if w.seqlens_k is None else
+                          torch.from_numpy(np.ascontiguousarray(w.seqlens_k, np.int32)).to(self.device))
+        nbytes = (0 if w.mask_kind == MASK_PAGED_PREFILL else
+                  attn.attn_workspace_bytes(w.B, w.Hq, w.Hkv, w.N, w.d, w.mask_kind, w.page_size))
         self.workspace = (torch.empty(max(nbytes, 16), dtype=torch.uint8, device=self.device)
                           if nbytes else None)
 
     def run(self, stream=None) -> int:
         w = self.w
+        if w.mask_kind == MASK_PAGED_PREFILL:
+            return attn.attn_fwd_paged_prefill(self.q, self.k, self.v, self.o, self.lse, w.B,
+                                               w.Hq, w.Hkv, w.N, w.d, w.scale, self.cu,
+                                               self.seqlens_k, self.table,
+                                               int(w.block_table.shape[1]), w.page_size,
+                                               self.num_pages, stream)
         return attn.attn_fwd(self.q, self.k, self.v, self.o, self.lse, w.B, w.Hq, w.Hkv, w.N, w.d,
                              w.scale, w.mask_kind, w.window, self.cu, self.table, w.page_size,
                              self.num_pages, self.workspace, stream)
