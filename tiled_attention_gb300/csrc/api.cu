@@ -130,6 +130,13 @@ bool document_kind(int m) { return m == ATTN_MASK_DOCUMENT || m == ATTN_MASK_DOC
 // 128-row prefill tile and either divide or are twice the 64-row decode stage.
 bool page_size_ok(int p) { return p == 16 || p == 32 || p == 64 || p == 128; }
 
+// log2 of a power of two (the page sizes page_size_ok accepts).
+int log2_exact(int p) {
+  int s = 0;
+  while ((1 << s) < p) ++s;
+  return s;
+}
+
 // The window argument: SLIDING needs >= 1 key, SLIDING_BIDIR >= 0 keys per side, PREFIX_LM a
 // prefix of >= 0 tokens; the other kinds ignore it.
 bool window_ok(int m, int window) {
@@ -328,7 +335,7 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
     p.Hkv = Hkv;
     p.max_pages = dense ? 0 : (N + page_size - 1) / page_size;
     p.num_pages = dense ? 0 : num_pages;
-    p.page_size = dense ? kDecodeStage : page_size;
+    p.page_shift = dense ? 6 : log2_exact(page_size);
     p.max_len = N;
     p.max_splits = L.max_splits;
     p.chunk_pages = kDecodeChunkPages;
@@ -424,6 +431,7 @@ int attn_fwd_paged_prefill(const void* q, const void* k, const void* v, void* o,
   p.table = block_table;
   p.max_pages = max_pages;
   p.page_size = page_size;
+  p.page_shift = log2_exact(page_size);
   p.num_pages = num_pages;
   p.B = B;
   p.Hq = Hq;

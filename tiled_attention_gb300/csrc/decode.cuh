@@ -44,7 +44,8 @@ struct DecodeParams {
   float* part_ml;        // [B*Hkv, max_splits, G, 2]
   int* counters;         // [B*Hkv], zero before the launch
   int B, Hq, Hkv, max_pages, num_pages, max_splits, chunk_pages;
-  int page_size;         // tokens per pool page (paged); a TMA box holds min(page_size, 64)
+  int page_shift;        // log2 of the tokens per pool page (paged: 4..7); a TMA box holds
+                         // min(page_size, 64) rows
   int dense;             // 1: K/V are dense caches [B*Hkv, max_len, D], no block table
   int max_len;           // longest valid context (N: the cache rows, or the table's reach)
   float scale_log2;
@@ -175,76 +176,90 @@ __global__ void __launch_bounds__(160, 2)
       prefetch_tensormap(&tm_k);
       prefetch_tensormap(&tm_v);
       const int* row = p.dense ? nullptr : p.table + static_cast<size_t>(b) * p.max_pages;
-      // Paged: stage k holds tokens 64 (pg0 + k) .. + 63 in boxes of `rows` tokens. The boxes'
-      // planes and first rows are looked up one stage ahead (table reads issued together), so
-      // their latency hides behind the current stage. A box whose first token is past the
-      // context, or whose table entry is outside the pool (never addressed; the status word
-      // reports it), is loaded from the plane just past the pool, which TMA fills with zeros,
-      // so the stage always receives its full bytes.
-      const int P = p.dense ? C::kPage : p.page_size;
-      const int rows = P < C::kPage ? P : C::kPage;
-      int pl[4], r0[4], pl_next[4], r0_next[4];
-      auto stage_boxes = [&](int k, int (&pl_o)[4], int (&r0_o)[4]) {
-        int raw[4];
-#pragma unroll
-        for (int sb = 0; sb < 4; ++sb) {
-          const int tok = (pg0 + k) * C::kPage + sb * rows;
-          raw[sb] = (sb < C::kPage / rows && tok < L) ? __ldg(row + tok / P) : -1;
-        }
-#pragma unroll
-        for (int sb = 0; sb < 4; ++sb) {
-          const int tok = (pg0 + k) * C::kPage + sb * rows;
-          pl_o[sb] = p.num_pages * p.Hkv;
-          r0_o[sb] = 0;
-          if (sb < C::kPage / rows && tok < L) {
-            if (raw[sb] < 0 || raw[sb] >= p.num_pages) {
+      const int lp = p.page_shift;  // log2(page_size)
+      int issued = 0;
+      if (p.dense || lp >= 6) {
+        // One box per stage: 64 rows of the dense cache, or the whole (P = 64) or one half
+        // (P = 128) of a page. A stage whose table entry is outside the pool (never addressed;
+        // the status word reports it) is loaded from the plane just past the pool, which TMA
+        // fills with zeros, so the stage always receives its full bytes.
+        for (int k = 0; k < n; ++k) {
+          const int st = k % S;
+          if (!mbar_wait(&ctl->empty[st], ((k / S) & 1) ^ 1, wc)) break;
+          ++issued;
+          uint8_t* dst = ring + st * C::kStageBytes;
+          const int tok = (pg0 + k) * C::kPage;
+          int plane, row0;
+          if (p.dense) {
+            // Rows past the cache's end read as zeros; rows past L_b are masked by the
+            // consumers.
+            plane = b * p.Hkv + g;
+            row0 = tok;
+          } else {
+            const int phys = row[tok >> lp];
+            row0 = tok & ((1 << lp) - 1);
+            plane = phys * p.Hkv + g;
+            if (phys < 0 || phys >= p.num_pages) {
               report_status(p.status, -5);
-            } else {
-              pl_o[sb] = raw[sb] * p.Hkv + g;
-              r0_o[sb] = tok % P;
+              plane = p.num_pages * p.Hkv;
             }
           }
-        }
-      };
-      if (!p.dense && n > 0) stage_boxes(0, pl_next, r0_next);
-      int issued = 0;
-      for (int k = 0; k < n; ++k) {
-        const int st = k % S;
-        if (!mbar_wait(&ctl->empty[st], ((k / S) & 1) ^ 1, wc)) break;
-        ++issued;
-        uint8_t* dst = ring + st * C::kStageBytes;
-        if (p.dense) {
-          // Page pg0 + k of the dense cache of (b, g): rows 64 (pg0 + k) .. + 63. Rows past
-          // the cache's end read as zeros; rows past L_b are masked by the consumers.
           mbar_arrive_expect_tx(&ctl->full[st], C::kStageBytes);
-          const int plane = b * p.Hkv + g;
 #pragma unroll
           for (int pn = 0; pn < C::kPanels; ++pn) {
-            tma_load_3d(dst + pn * C::kPanelBytes, &tm_k, &ctl->full[st], pn * 64,
-                        (pg0 + k) * C::kPage, plane);
+            tma_load_3d(dst + pn * C::kPanelBytes, &tm_k, &ctl->full[st], pn * 64, row0, plane);
             tma_load_3d(dst + C::kPageBytes + pn * C::kPanelBytes, &tm_v, &ctl->full[st],
-                        pn * 64, (pg0 + k) * C::kPage, plane);
-          }
-          continue;
-        }
-#pragma unroll
-        for (int sb = 0; sb < 4; ++sb) {
-          pl[sb] = pl_next[sb];
-          r0[sb] = r0_next[sb];
-        }
-        mbar_arrive_expect_tx(&ctl->full[st], C::kStageBytes);
-#pragma unroll
-        for (int sb = 0; sb < 4; ++sb) {
-          if (sb >= C::kPage / rows) break;
-#pragma unroll
-          for (int pn = 0; pn < C::kPanels; ++pn) {
-            tma_load_3d(dst + pn * C::kPanelBytes + sb * rows * 128, &tm_k, &ctl->full[st],
-                        pn * 64, r0[sb], pl[sb]);
-            tma_load_3d(dst + C::kPageBytes + pn * C::kPanelBytes + sb * rows * 128, &tm_v,
-                        &ctl->full[st], pn * 64, r0[sb], pl[sb]);
+                        pn * 64, row0, plane);
           }
         }
-        if (k + 1 < n) stage_boxes(k + 1, pl_next, r0_next);
+      } else {
+        // Pages of 16 or 32 tokens: stage k is 64 >> lp whole pages. Their planes are looked
+        // up one stage ahead (table reads issued together), so the lookup latency hides
+        // behind the current stage. A page past the context, or whose table entry is outside
+        // the pool, is loaded from the zero-filled plane past the pool.
+        const int nb = C::kPage >> lp;  // boxes per stage (4 or 2)
+        int pl[4], pl_next[4];
+        auto stage_planes = [&](int k, int (&out)[4]) {
+          int raw[4];
+#pragma unroll
+          for (int sb = 0; sb < 4; ++sb) {
+            const int tok = (pg0 + k) * C::kPage + (sb << lp);
+            raw[sb] = (sb < nb && tok < L) ? __ldg(row + (tok >> lp)) : -1;
+          }
+#pragma unroll
+          for (int sb = 0; sb < 4; ++sb) {
+            const int tok = (pg0 + k) * C::kPage + (sb << lp);
+            out[sb] = p.num_pages * p.Hkv;
+            if (sb < nb && tok < L) {
+              if (raw[sb] < 0 || raw[sb] >= p.num_pages)
+                report_status(p.status, -5);
+              else
+                out[sb] = raw[sb] * p.Hkv + g;
+            }
+          }
+        };
+        if (n > 0) stage_planes(0, pl_next);
+        for (int k = 0; k < n; ++k) {
+          const int st = k % S;
+          if (!mbar_wait(&ctl->empty[st], ((k / S) & 1) ^ 1, wc)) break;
+          ++issued;
+          uint8_t* dst = ring + st * C::kStageBytes;
+#pragma unroll
+          for (int sb = 0; sb < 4; ++sb) pl[sb] = pl_next[sb];
+          mbar_arrive_expect_tx(&ctl->full[st], C::kStageBytes);
+#pragma unroll
+          for (int sb = 0; sb < 4; ++sb) {
+            if (sb >= nb) break;
+#pragma unroll
+            for (int pn = 0; pn < C::kPanels; ++pn) {
+              tma_load_3d(dst + pn * C::kPanelBytes + (sb << lp) * 128, &tm_k, &ctl->full[st],
+                          pn * 64, 0, pl[sb]);
+              tma_load_3d(dst + C::kPageBytes + pn * C::kPanelBytes + (sb << lp) * 128, &tm_v,
+                          &ctl->full[st], pn * 64, 0, pl[sb]);
+            }
+          }
+          if (k + 1 < n) stage_planes(k + 1, pl_next);
+        }
       }
       for (int k = imax(0, issued - S); k < issued; ++k)
         mbar_wait(&ctl->full[k % S], (k / S) & 1, wc_drain);

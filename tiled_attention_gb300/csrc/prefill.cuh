@@ -48,7 +48,7 @@ struct PrefillParams {
   const int* cu_seqlens;    // packed kinds: [B+1] segment / query-chunk starts
   const int* seqlens_k;     // PAGED_PREFILL: [B] context lengths (each chunk included)
   const int* table;         // PAGED_PREFILL: [B, max_pages] block table
-  int max_pages, page_size, num_pages;  // PAGED_PREFILL
+  int max_pages, page_size, page_shift, num_pages;  // PAGED_PREFILL (page_size = 1 << shift)
   int B, Hq, Hkv, N, group; // N: rows per (batch, head) plane (T for DOCUMENT)
   int num_units;            // work units; DOCUMENT: an upper bound (surplus ones decode invalid)
   int window;               // SLIDING / SLIDING_BIDIR window, PREFIX_LM prefix length
@@ -355,20 +355,21 @@ __global__ void __launch_bounds__(384, 1)
           // fills with zeros, so the stage always receives its full bytes.
           int pl[8], pl_next[8];
           auto page_planes = [&](int j, int (&out)[8]) {
-            const int P = p.page_size;
+            const int lp = p.page_shift;
+            const int nb = BN >> lp;
             const int lk = un.k_end - un.k_org;
             const int* trow = p.table + static_cast<size_t>(un.seq) * p.max_pages;
             int raw[8];
 #pragma unroll
             for (int sb = 0; sb < 8; ++sb) {
-              const int tok = j * BN + sb * P;
-              raw[sb] = (sb < BN / P && tok < lk) ? __ldg(trow + tok / P) : -1;
+              const int tok = j * BN + (sb << lp);
+              raw[sb] = (sb < nb && tok < lk) ? __ldg(trow + (tok >> lp)) : -1;
             }
 #pragma unroll
             for (int sb = 0; sb < 8; ++sb) {
-              const int tok = j * BN + sb * P;
+              const int tok = j * BN + (sb << lp);
               out[sb] = p.num_pages * p.Hkv;
-              if (sb < BN / P && tok < lk) {
+              if (sb < nb && tok < lk) {
                 if (raw[sb] < 0 || raw[sb] >= p.num_pages)
                   report_status(p.status, -5);
                 else
@@ -386,17 +387,17 @@ __global__ void __launch_bounds__(384, 1)
             const CUtensorMap* m = (x & 1) ? &tm_v : &tm_k;
             uint8_t* dst = kv_s + st * C::kKVBytes;
             if (MASK == kMaskPagedPrefill) {
-              const int P = p.page_size;
+              const int lp = p.page_shift;
               if (!(x & 1)) {
 #pragma unroll
                 for (int sb = 0; sb < 8; ++sb) pl[sb] = pl_next[sb];
               }
 #pragma unroll
               for (int sb = 0; sb < 8; ++sb) {
-                if (sb >= BN / P) break;
+                if (sb >= (BN >> lp)) break;
                 for (int c = 0; c < C::kPanels; ++c)
-                  tma_load_3d(dst + c * C::kChunkBytes + sb * P * 128, m, &ctl->kv_full[st],
-                              c * 64, 0, pl[sb]);
+                  tma_load_3d(dst + c * C::kChunkBytes + (sb << lp) * 128, m,
+                              &ctl->kv_full[st], c * 64, 0, pl[sb]);
               }
               if (!(x & 1) && lo + x / 2 + 1 < hi) page_planes(lo + x / 2 + 1, pl_next);
             } else {
