@@ -46,6 +46,8 @@ def _load(path: str = None):
         lib.oracle_attn.argtypes = [p, p, p, i, i, i, i, i, ctypes.c_float, i, i, p, p, p, i,
                                     i, p, i64, p, p, p, i64, i]
         lib.oracle_attn.restype = i
+        lib.oracle_attn_qk_f64.argtypes = lib.oracle_attn.argtypes
+        lib.oracle_attn_qk_f64.restype = i
         lib.oracle_max_threads.argtypes = [i]
         lib.oracle_max_threads.restype = i
         _libs[path] = lib
@@ -61,15 +63,28 @@ def max_threads(threads: int = 0) -> int:
 
 
 def attention(w, rows=None, probs: bool = False, threads: int = 0, lib_path: str = None):
-    """Run the oracle on a ``tiled_attention_gb300.inputs.Workload``-shaped problem.
+    """Run the oracle on a ``tiled_attention_gb300.inputs.Workload``-shaped problem. A
+    workload carrying FP8 Q / K (``q8``, ``k8``, ``q_scales``, ``k_scales``) is computed on
+    their dequantized values.
 
     rows: optional int64 array of flattened output-row indices (output order of O / LSE);
     default all rows. Returns (o [nrows, d] float64, lse [nrows] float64[, probs]).
     lib_path: another build of an oracle source (the mutation tests use this).
     """
     lib = _load(lib_path)
-    q = np.ascontiguousarray(w.q, dtype=np.uint16)
-    k = np.ascontiguousarray(w.k, dtype=np.uint16)
+    fp8 = getattr(w, "q8", None) is not None
+    if fp8:
+        # FP8 Q / K: the dequantized blocks (code value x block scale), exact in float64.
+        from . import fp8 as _fp8
+        q = np.ascontiguousarray(_fp8.dequantize(w.q8.reshape(-1, w.q8.shape[-2], w.d),
+                                                 w.q_scales.reshape(-1, w.q_scales.shape[-1])))
+        k = np.ascontiguousarray(_fp8.dequantize(w.k8.reshape(-1, w.k8.shape[-2], w.d),
+                                                 w.k_scales.reshape(-1, w.k_scales.shape[-1])))
+        entry = lib.oracle_attn_qk_f64
+    else:
+        q = np.ascontiguousarray(w.q, dtype=np.uint16)
+        k = np.ascontiguousarray(w.k, dtype=np.uint16)
+        entry = lib.oracle_attn
     v = np.ascontiguousarray(w.v, dtype=np.uint16)
     cu = None if w.cu_seqlens is None else np.ascontiguousarray(w.cu_seqlens, dtype=np.int32)
     tab = None if w.block_table is None else np.ascontiguousarray(w.block_table, dtype=np.int32)
@@ -92,7 +107,7 @@ def attention(w, rows=None, probs: bool = False, threads: int = 0, lib_path: str
     else:
         nk = w.N
     pr = np.zeros((n, max(nk, 1)), dtype=np.float64) if probs else None
-    rc = lib.oracle_attn(_ptr(q), _ptr(k), _ptr(v), w.B, w.Hq, w.Hkv, w.N, w.d,
+    rc = entry(_ptr(q), _ptr(k), _ptr(v), w.B, w.Hq, w.Hkv, w.N, w.d,
                          ctypes.c_float(w.scale), w.mask_kind, w.window, _ptr(cu), _ptr(lk),
                          _ptr(tab), max_pages, w.page_size, _ptr(rows_arr), n, _ptr(o), _ptr(lse),
                          _ptr(pr), pr.shape[1] if probs else 0, threads)

@@ -74,6 +74,7 @@ static int is_paged(int mask) { return mask == OR_PAGED || mask == OR_PAGED_PREF
 
 typedef struct {
     const uint16_t *q, *k, *v;
+    const double *qd, *kd;  /* when set, Q and K are these fp64 values instead of q / k */
     int B, Hq, Hkv, N, d;
     double s;
     int mask, W;
@@ -142,20 +143,29 @@ static int visible(const problem_t *P, int b, int i, int j) {
     return 0;
 }
 
-static const uint16_t *query_row(const problem_t *P, int b, int h, int i) {
-    if (is_decode(P->mask)) return P->q + ((size_t)b * P->Hq + h) * P->d;
-    if (is_document(P->mask)) return P->q + ((size_t)h * P->N + i) * P->d;
-    return P->q + (((size_t)b * P->Hq + h) * P->N + i) * P->d;
+/* Element offset of query row (b, h, i). */
+static size_t query_row(const problem_t *P, int b, int h, int i) {
+    if (is_decode(P->mask)) return ((size_t)b * P->Hq + h) * P->d;
+    if (is_document(P->mask)) return ((size_t)h * P->N + i) * P->d;
+    return (((size_t)b * P->Hq + h) * P->N + i) * P->d;
 }
 
-/* Key or value row j of (b, g); base is the k or the v tensor. */
-static const uint16_t *kv_row(const problem_t *P, const uint16_t *base, int b, int g, int j) {
+/* Element offset of key / value row j of (b, g) (k and v share the layout). */
+static size_t kv_row(const problem_t *P, int b, int g, int j) {
     if (is_paged(P->mask)) {
         int phys = P->table[(size_t)b * P->max_pages + j / P->page];
-        return base + ((((size_t)phys * P->Hkv + g) * P->page) + (size_t)(j % P->page)) * P->d;
+        return ((((size_t)phys * P->Hkv + g) * P->page) + (size_t)(j % P->page)) * P->d;
     }
-    if (is_document(P->mask)) return base + ((size_t)g * P->N + j) * P->d;
-    return base + (((size_t)b * P->Hkv + g) * P->N + j) * P->d;
+    if (is_document(P->mask)) return ((size_t)g * P->N + j) * P->d;
+    return (((size_t)b * P->Hkv + g) * P->N + j) * P->d;
+}
+
+static double q_at(const problem_t *P, size_t off) {
+    return P->qd ? P->qd[off] : widen_bf16(P->q[off]);
+}
+
+static double k_at(const problem_t *P, size_t off) {
+    return P->kd ? P->kd[off] : widen_bf16(P->k[off]);
 }
 
 /* One query row from the definition. z is scratch of key_count() doubles; probs (optional)
@@ -166,15 +176,15 @@ static void attend_row(const problem_t *P, int64_t r, double *z, double *o, doub
     row_coords(P, r, &b, &h, &i);
     const int g = h / (P->Hq / P->Hkv);
     const int nk = key_count(P, b);
-    const uint16_t *qr = query_row(P, b, h, i);
+    const size_t qr = query_row(P, b, h, i);
 
     double M = -INFINITY;
     int any = 0;
     for (int j = 0; j < nk; j++) {
         if (!visible(P, b, i, j)) continue;
-        const uint16_t *kr = kv_row(P, P->k, b, g, j);
+        const size_t kr = kv_row(P, b, g, j);
         double dot = 0.0;
-        for (int c = 0; c < P->d; c++) dot += widen_bf16(qr[c]) * widen_bf16(kr[c]);
+        for (int c = 0; c < P->d; c++) dot += q_at(P, qr + c) * k_at(P, kr + c);
         z[j] = P->s * dot;
         if (z[j] > M) M = z[j];
         any = 1;
@@ -195,7 +205,7 @@ static void attend_row(const problem_t *P, int64_t r, double *z, double *o, doub
             continue;
         }
         const double e = exp(z[j] - M);
-        const uint16_t *vr = kv_row(P, P->v, b, g, j);
+        const uint16_t *vr = P->v + kv_row(P, b, g, j);
         for (int c = 0; c < P->d; c++) o[c] += e * widen_bf16(vr[c]);
         if (probs) probs[j] = e / l;
     }
@@ -208,13 +218,13 @@ static void attend_row(const problem_t *P, int64_t r, double *z, double *o, doub
  * o: nrows x d doubles; lse: nrows doubles; probs (optional): nrows x probs_stride doubles.
  * Returns 0, or -1 for arguments the definition does not cover.
  */
-int oracle_attn(const uint16_t *q, const uint16_t *k, const uint16_t *v, int B, int Hq,
-                int Hkv, int N, int d, float scale, int mask_kind, int window,
-                const int32_t *cu_seqlens, const int32_t *seqlens_k,
-                const int32_t *block_table, int max_pages, int page_size, const int64_t *rows,
-                int64_t nrows, double *o, double *lse, double *probs, int64_t probs_stride,
-                int nthreads) {
-    problem_t P = {q, k, v, B, Hq, Hkv, N, d, (double)scale, mask_kind, window,
+static int oracle_run(const uint16_t *q, const uint16_t *k, const double *qd, const double *kd,
+                      const uint16_t *v, int B, int Hq, int Hkv, int N, int d, float scale,
+                      int mask_kind, int window, const int32_t *cu_seqlens,
+                      const int32_t *seqlens_k, const int32_t *block_table, int max_pages,
+                      int page_size, const int64_t *rows, int64_t nrows, double *o, double *lse,
+                      double *probs, int64_t probs_stride, int nthreads) {
+    problem_t P = {q, k, v, qd, kd, B, Hq, Hkv, N, d, (double)scale, mask_kind, window,
                    cu_seqlens, seqlens_k, block_table, max_pages, page_size};
     if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || d <= 0 || N < 0) return -1;
     if (mask_kind < OR_NONE || mask_kind > OR_PAGED_PREFILL) return -1;
@@ -270,6 +280,31 @@ int oracle_attn(const uint16_t *q, const uint16_t *k, const uint16_t *v, int B, 
         free(z);
     }
     return failed ? -2 : 0;
+}
+
+int oracle_attn(const uint16_t *q, const uint16_t *k, const uint16_t *v, int B, int Hq,
+                int Hkv, int N, int d, float scale, int mask_kind, int window,
+                const int32_t *cu_seqlens, const int32_t *seqlens_k,
+                const int32_t *block_table, int max_pages, int page_size, const int64_t *rows,
+                int64_t nrows, double *o, double *lse, double *probs, int64_t probs_stride,
+                int nthreads) {
+    return oracle_run(q, k, NULL, NULL, v, B, Hq, Hkv, N, d, scale, mask_kind, window,
+                      cu_seqlens, seqlens_k, block_table, max_pages, page_size, rows, nrows, o,
+                      lse, probs, probs_stride, nthreads);
+}
+
+/* The same with Q and K given as fp64 values (the FP8 path passes its dequantized blocks,
+ * code value times block scale, which fp64 holds exactly); V stays bf16. */
+int oracle_attn_qk_f64(const double *q, const double *k, const uint16_t *v, int B, int Hq,
+                       int Hkv, int N, int d, float scale, int mask_kind, int window,
+                       const int32_t *cu_seqlens, const int32_t *seqlens_k,
+                       const int32_t *block_table, int max_pages, int page_size,
+                       const int64_t *rows, int64_t nrows, double *o, double *lse,
+                       double *probs, int64_t probs_stride, int nthreads) {
+    if (!q || !k) return -1;
+    return oracle_run(NULL, NULL, q, k, v, B, Hq, Hkv, N, d, scale, mask_kind, window,
+                      cu_seqlens, seqlens_k, block_table, max_pages, page_size, rows, nrows, o,
+                      lse, probs, probs_stride, nthreads);
 }
 
 /* Number of OpenMP threads a parallel region would use (for reporting the CPU baseline). */

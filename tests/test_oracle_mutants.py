@@ -19,8 +19,8 @@ MUTANTS = [
     ("document_not_causal", "return j <= i && j >= P->cu[b];",
      "return j < P->cu[b + 1] && j >= P->cu[b];"),
     ("gqa_modulo", "const int g = h / (P->Hq / P->Hkv);", "const int g = h % P->Hkv;"),
-    ("kv_batch_head_swapped", "return base + (((size_t)b * P->Hkv + g) * P->N + j) * P->d;",
-     "return base + (((size_t)g * P->B + b) * P->N + j) * P->d;"),
+    ("kv_batch_head_swapped", "return (((size_t)b * P->Hkv + g) * P->N + j) * P->d;",
+     "return (((size_t)g * P->B + b) * P->N + j) * P->d;"),
     ("paged_slot", "(size_t)(j % P->page)) * P->d;", "(size_t)(j / P->page)) * P->d;"),
     ("paged_length", "case OR_DECODE: return j < P->cu[b + 1] - P->cu[b];",
      "case OR_DECODE: return j <= P->cu[b + 1] - P->cu[b] - 2;"),
@@ -47,8 +47,8 @@ MUTANTS = [
     ("paged_prefill_strict",
      "return j < Lk && j <= (i - P->cu[b]) + (Lk - Lq);",
      "return j < Lk && j < (i - P->cu[b]) + (Lk - Lq);"),
-    ("query_transposed", "return P->q + (((size_t)b * P->Hq + h) * P->N + i) * P->d;",
-     "return P->q + (((size_t)b * P->Hq + h) * P->N) * P->d + i;"),
+    ("query_transposed", "return (((size_t)b * P->Hq + h) * P->N + i) * P->d;",
+     "return (((size_t)b * P->Hq + h) * P->N) * P->d + i;"),
 ]
 
 

@@ -108,6 +108,12 @@ class Workload:
     block_table: Optional[np.ndarray] = None
     page_size: int = 0
     seqlens_k: Optional[np.ndarray] = None
+    # FP8 Q / K (E4M3 codes in the q / k layouts) and their per-128-row block scales
+    # [planes, ceil(N/128)]; when set, q8 / k8 replace q / k as the attention inputs.
+    q8: Optional[np.ndarray] = None
+    k8: Optional[np.ndarray] = None
+    q_scales: Optional[np.ndarray] = None
+    k_scales: Optional[np.ndarray] = None
 
     @property
     def out_shape(self):
