@@ -302,6 +302,39 @@ def suite(args):
                 "unit": "GB/s (valid K+V per decode)",
                 "value": dec_bytes(w) / (both_ms * 1e-3) / 1e9}), flush=True)
             del kd, vd, ws
+        if cfg == "3c":
+            # FP8 path on the same shape: Q and K block-quantized to E4M3 by the library (timed
+            # on its own), then attention with S = Q K^T on the FP8 tensor cores. Half the
+            # FLOPs (Q K^T) run at the FP8 rate, twice the bf16 one, so the peak for the whole
+            # is 4/3 of the bf16 peak.
+            B, Hq, Hkv, N, d = w.B, w.Hq, w.Hkv, w.N, w.d
+            q8 = torch.empty((B, Hq, N, d), dtype=torch.uint8, device=dev)
+            k8 = torch.empty((B, Hkv, N, d), dtype=torch.uint8, device=dev)
+            qs = torch.empty((B * Hq, (N + 127) // 128), dtype=torch.float32, device=dev)
+            ks = torch.empty((B * Hkv, (N + 127) // 128), dtype=torch.float32, device=dev)
+
+            def quant():
+                rc = attn.attn_quantize_fp8(dp.q, q8, qs, B * Hq, N, d, stream)
+                return rc | attn.attn_quantize_fp8(dp.k, k8, ks, B * Hkv, N, d, stream)
+
+            def fwd8():
+                return attn.attn_fwd_fp8(q8, k8, dp.v, dp.o, dp.lse, qs, ks, B, Hq, Hkv, N, d,
+                                         w.scale, w.mask_kind, w.window, stream)
+
+            q_ms = timed(quant, args.steps)
+            f_ms = timed(fwd8, args.steps)
+            tf = w.flops() / (f_ms * 1e-3) / 1e12
+            qbytes = (dp.q.numel() + dp.k.numel()) * 3 + (qs.numel() + ks.numel()) * 4
+            print(json.dumps({
+                "suite": True, "workload": "FP8 Q/K (E4M3, 128-row tile scales) " + w.name,
+                "mask_kind": w.mask_kind, "d": d, "ms": f_ms, "launches_timed": args.steps,
+                "value": tf, "unit": "TFLOP/s",
+                "frac": tf / (peaks["bf16_tflops"] * 4 / 3),
+                "peak": f"4/3 x bf16 burst {tag} (Q K^T at the FP8 rate, P V at bf16)",
+                "frac_of_bf16_peak": tf / peaks["bf16_tflops"], "flops": w.flops(),
+                "quantize_ms": q_ms,
+                "quantize_gbs": qbytes / (q_ms * 1e-3) / 1e9}), flush=True)
+            del q8, k8, qs, ks
         del dp
         torch.cuda.empty_cache()
 

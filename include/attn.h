@@ -155,6 +155,43 @@ int attn_fwd_paged_prefill(const void *q, const void *k, const void *v, void *o,
                            const int32_t *block_table, int max_pages, int page_size,
                            int num_pages, void *stream);
 
+/*
+ * attn_quantize_fp8 — FP8 E4M3 block quantization of a bf16 tensor x [planes, N, d].
+ *
+ * The block quantization of "FlashAttention-3: Warp Specialization and the 75% FLOPS Barrier on
+ * Hopper" ("FP8 Block Quantization"), with one scale per 128-row tile of a plane (the page's
+ * prose says per tile): for rows [128t, min(128t + 128, N)) of plane p,
+ *   scales[p][t] = amax / 448                      (fp32, IEEE division; 0 if amax is 0)
+ *   x8[p][r][c]  = E4M3(x[p][r][c] / scales[p][t]) (IEEE fp32 division, round to nearest even,
+ *                                                   saturating; 0 when the scale is 0)
+ * x     bf16 [planes, N, d], 16-byte aligned (device).
+ * x8    E4M3 bytes [planes, N, d], 16-byte aligned (device, written).
+ * scales fp32 [planes, ceil(N/128)] (device, written).
+ * d 64 or 128; planes <= 65535. Asynchronous on `stream`.
+ */
+int attn_quantize_fp8(const void *x, void *x8, float *scales, int planes, int N, int d,
+                      void *stream);
+
+/*
+ * attn_fwd_fp8 — attention forward with E4M3 Q and K (the FP8 path of the same page).
+ *
+ * Same result definition as attn_fwd, with Q and K replaced by their dequantized blocks:
+ * q[b,h,i,:] = q8[b,h,i,:] * q_scales[b*Hq + h][i / 128] and likewise for k. S = Q K^T runs on
+ * the FP8 tensor cores (fp32 accumulation); the two tile scales join the softmax's per-tile
+ * scale, so the rescale after the matmul costs nothing per element. V, P and O stay bf16.
+ * q8        E4M3 [B, Hq, N, 128]; k8 E4M3 [B, Hkv, N, 128]; v bf16 [B, Hkv, N, 128].
+ * o, lse    as attn_fwd (bf16 [B, Hq, N, 128], fp32 [B, Hq, N]).
+ * q_scales  fp32 [B*Hq, ceil(N/128)]; k_scales fp32 [B*Hkv, ceil(N/128)] (attn_quantize_fp8's
+ *           layout). Finite and >= 0 (a 0 scale means an all-zero tile).
+ * d         128 only (else ATTN_ERR_UNSUPPORTED).
+ * mask_kind NONE, CAUSAL, SLIDING, SLIDING_BIDIR or PREFIX_LM (the document, paged and decode
+ *           kinds return ATTN_ERR_UNSUPPORTED); window as for attn_fwd.
+ * No workspace; asynchronous on `stream`.
+ */
+int attn_fwd_fp8(const void *q8, const void *k8, const void *v, void *o, float *lse,
+                 const float *q_scales, const float *k_scales, int B, int Hq, int Hkv, int N,
+                 int d, float scale, int mask_kind, int window, void *stream);
+
 /* Bytes of workspace attn_fwd needs for these arguments (0 for the prefill kinds; DECODE
  * ignores page_size). */
 size_t attn_workspace_bytes(int B, int Hq, int Hkv, int N, int d, int mask_kind, int page_size);

@@ -143,6 +143,29 @@ def test_paged_decode_page_sizes():
     assert len(sizes) == 1
 
 
+def test_fp8_validation_before_cuda():
+    t = _FakeDevicePtr()
+    base = dict(q8=t, k8=t, v=t, o=t, lse=t, q_scales=t, k_scales=t, B=1, Hq=4, Hkv=2, N=256,
+                d=128, scale=0.1, mask_kind=CAUSAL, window=0, stream=0)
+
+    def call(**kw):
+        a = dict(base)
+        a.update(kw)
+        return attn.attn_fwd_fp8(**a)
+    assert call(d=64) == attn.ATTN_ERR_UNSUPPORTED
+    assert call(mask_kind=DOCUMENT) == attn.ATTN_ERR_UNSUPPORTED
+    assert call(mask_kind=attn.ATTN_MASK_PAGED_DECODE) == attn.ATTN_ERR_UNSUPPORTED
+    assert call(mask_kind=42) == attn.ATTN_ERR_INVALID
+    assert call(q_scales=None) == attn.ATTN_ERR_INVALID
+    assert call(mask_kind=SLIDING, window=0) == attn.ATTN_ERR_INVALID
+    assert call(Hq=3) == attn.ATTN_ERR_INVALID
+    assert call(B=0) == attn.ATTN_OK
+    assert attn.attn_quantize_fp8(t, t, t, 4, 100, 96, 0) == attn.ATTN_ERR_UNSUPPORTED
+    assert attn.attn_quantize_fp8(t, t, t, 70000, 100, 128, 0) == attn.ATTN_ERR_UNSUPPORTED
+    assert attn.attn_quantize_fp8(None, t, t, 4, 100, 128, 0) == attn.ATTN_ERR_INVALID
+    assert attn.attn_quantize_fp8(t, t, t, 0, 100, 128, 0) == attn.ATTN_OK
+
+
 def test_workspace_bytes():
     assert attn.attn_workspace_bytes(4, 16, 16, 2048, 128, CAUSAL, 0) == 0
     n = attn.attn_workspace_bytes(32, 32, 8, 16384, 128, 4, 64)

@@ -43,6 +43,9 @@ _SIGS = {
                       _i, _p, ctypes.c_size_t, _p]),
     "attn_fwd_paged_prefill": (_i, [_p, _p, _p, _p, _p, _i, _i, _i, _i, _i, ctypes.c_float, _p,
                                     _p, _p, _i, _i, _i, _p]),
+    "attn_quantize_fp8": (_i, [_p, _p, _p, _i, _i, _i, _p]),
+    "attn_fwd_fp8": (_i, [_p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, ctypes.c_float, _i, _i,
+                          _p]),
     "attn_workspace_bytes": (ctypes.c_size_t, [_i, _i, _i, _i, _i, _i, _i]),
     "attn_gather_pages": (_i, [_p, _p, _p, _i, _i, _i, _i, _i, _i, _p]),
     "attn_get_status": (_i, [_p]),
@@ -129,6 +132,20 @@ def attn_fwd_paged_prefill(q, k, v, o, lse, B, Hq, Hkv, total_q, d, scale, cu_se
                                         Hkv, total_q, d, ctypes.c_float(scale),
                                         _ptr(cu_seqlens_q), _ptr(seqlens_k), _ptr(block_table),
                                         max_pages, page_size, num_pages, _stream(stream))
+
+
+def attn_quantize_fp8(x, x8, scales, planes, N, d, stream=None) -> int:
+    """E4M3 block quantization of a bf16 tensor [planes, N, d] (torch tensors on the device)."""
+    return lib().attn_quantize_fp8(_ptr(x), _ptr(x8), _ptr(scales), planes, N, d,
+                                   _stream(stream))
+
+
+def attn_fwd_fp8(q8, k8, v, o, lse, q_scales, k_scales, B, Hq, Hkv, N, d, scale, mask_kind,
+                 window=0, stream=None) -> int:
+    """Attention with E4M3 Q / K and per-128-row-tile scales (torch tensors on the device)."""
+    return lib().attn_fwd_fp8(_ptr(q8), _ptr(k8), _ptr(v), _ptr(o), _ptr(lse), _ptr(q_scales),
+                              _ptr(k_scales), B, Hq, Hkv, N, d, ctypes.c_float(scale),
+                              mask_kind, window, _stream(stream))
 
 
 def attn_paged_decode_noalloc(q, k, v, o, lse, B, Hq, Hkv, N, d, scale, cu_seqlens, block_table,

@@ -115,6 +115,24 @@ int encode_3d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, u
   return ATTN_OK;
 }
 
+// 3-D E4M3 (byte) view [planes][rows][inner] with a 128-column x box_rows box, 128-byte
+// swizzle: one box row is one 128-byte swizzle row, as for the bf16 maps' 64 columns.
+int encode_3d_u8(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows,
+                 uint64_t planes, uint32_t box_rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc;
+  int rc = get_encoder(&enc);
+  if (rc) return rc;
+  cuuint64_t dims[3] = {inner, rows, planes};
+  cuuint64_t strides[2] = {inner, inner * rows};
+  cuuint32_t box[3] = {128, box_rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled (u8) failed (%d)", (int)r);
+  return ATTN_OK;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Mask kinds served by the prefill kernel.
@@ -199,6 +217,67 @@ __global__ void gather_pages_kernel(const uint4* __restrict__ pool, uint4* __res
     const uint4* src = pool + (static_cast<size_t>(phys) * Hkv + g) * page_vec;
     uint4* out = dst + ((static_cast<size_t>(b) * Hkv + g) * max_pages + p) * page_vec;
     for (int i = static_cast<int>(threadIdx.x); i < page_vec; i += blockDim.x) out[i] = src[i];
+  }
+}
+
+// ------------------------------------------------------------------ FP8 block quantization
+// One CTA per (128-row block, plane) of x [planes, N, d] (bf16): amax over the block's rows,
+// scale = amax / 448 (IEEE fp32 division; 448 is the largest finite E4M3 value), codes =
+// E4M3(x / scale) rounded to nearest even with saturation, the division again IEEE fp32. An
+// all-zero block gets scale 0 and zero codes. This is the block quantization of the
+// FlashAttention-3 page ("FP8 Block Quantization"), one scale per 128-row tile.
+constexpr int kFp8Block = 128;
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Two fp32 -> E4M3 codes in one 16-bit word, `lo` in the low byte.
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+__global__ void __launch_bounds__(256)
+    quantize_fp8_kernel(const uint4* __restrict__ x, uint2* __restrict__ x8,
+                        float* __restrict__ scales, int N, int d, int nb) {
+  const int t = static_cast<int>(blockIdx.x);
+  const int pl = static_cast<int>(blockIdx.y);
+  const int r0 = t * kFp8Block;
+  const int rows = imin(kFp8Block, N - r0);
+  const size_t base = (static_cast<size_t>(pl) * N + r0) * d / 8;  // 8-element vectors
+  const int nvec = rows * d / 8;
+  __shared__ float red[8];
+  __shared__ float s_scale;
+  float amax = 0.f;
+  for (int i = static_cast<int>(threadIdx.x); i < nvec; i += blockDim.x) {
+    const uint4 v = x[base + i];
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(w[e])), fabsf(bf16_hi(w[e]))));
+  }
+  for (int off = 16; off; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float m = red[0];
+    for (int w = 1; w < static_cast<int>(blockDim.x >> 5); ++w) m = fmaxf(m, red[w]);
+    const float sc = __fdiv_rn(m, 448.f);
+    s_scale = sc;
+    scales[static_cast<size_t>(pl) * nb + t] = sc;
+  }
+  __syncthreads();
+  const float sc = s_scale;
+  for (int i = static_cast<int>(threadIdx.x); i < nvec; i += blockDim.x) {
+    const uint4 v = x[base + i];
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t c[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      c[e] = sc == 0.f ? 0u
+                       : e4m3x2(__fdiv_rn(bf16_lo(w[e]), sc), __fdiv_rn(bf16_hi(w[e]), sc));
+    x8[base + i] = make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
   }
 }
 
@@ -450,6 +529,84 @@ int attn_fwd_paged_prefill(const void* q, const void* k, const void* v, void* o,
   cudaError_t e = d == 64 ? launch_prefill_d64(kMaskPagedPrefill, tq, tk, tv, to, p, grid, st)
                           : launch_prefill_d128(kMaskPagedPrefill, tq, tk, tv, to, p, grid, st);
   if (e != cudaSuccess) return cuda_fail(e, "paged prefill launch");
+  return ATTN_OK;
+}
+
+int attn_quantize_fp8(const void* x, void* x8, float* scales, int planes, int N, int d,
+                      void* stream) {
+  g_last_error.clear();
+  if (planes < 0 || N < 0) return fail(ATTN_ERR_INVALID, "planes %d, N %d", planes, N);
+  if (d != 64 && d != 128) return fail(ATTN_ERR_UNSUPPORTED, "head dim %d (64 or 128)", d);
+  if (planes == 0 || N == 0) return ATTN_OK;
+  if (!x || !x8 || !scales) return fail(ATTN_ERR_INVALID, "null pointer");
+  if (!aligned16(x) || !aligned16(x8) || (reinterpret_cast<uintptr_t>(scales) & 3u))
+    return fail(ATTN_ERR_INVALID, "x and x8 must be 16-byte aligned, scales 4-byte aligned");
+  if (planes > 65535) return fail(ATTN_ERR_UNSUPPORTED, "planes %d > 65535", planes);
+  const int nb = (N + kFp8Block - 1) / kFp8Block;
+  quantize_fp8_kernel<<<dim3(nb, planes), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<const uint4*>(x), static_cast<uint2*>(x8), scales, N, d, nb);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "quantize launch");
+  return ATTN_OK;
+}
+
+int attn_fwd_fp8(const void* q8, const void* k8, const void* v, void* o, float* lse,
+                 const float* q_scales, const float* k_scales, int B, int Hq, int Hkv, int N,
+                 int d, float scale, int mask_kind, int window, void* stream) {
+  g_last_error.clear();
+  if (mask_kind < ATTN_MASK_NONE || mask_kind > ATTN_MASK_PAGED_PREFILL)
+    return fail(ATTN_ERR_INVALID, "unknown mask_kind %d", mask_kind);
+  if (mask_kind != ATTN_MASK_NONE && mask_kind != ATTN_MASK_CAUSAL &&
+      mask_kind != ATTN_MASK_SLIDING && mask_kind != ATTN_MASK_SLIDING_BIDIR &&
+      mask_kind != ATTN_MASK_PREFIX_LM)
+    return fail(ATTN_ERR_UNSUPPORTED, "FP8 takes the dense mask kinds (not %d)", mask_kind);
+  if (B < 0 || N < 0 || Hq <= 0 || Hkv <= 0)
+    return fail(ATTN_ERR_INVALID, "need B >= 0, N >= 0, Hq > 0, Hkv > 0");
+  if (Hq % Hkv != 0) return fail(ATTN_ERR_INVALID, "Hq (%d) %% Hkv (%d) != 0", Hq, Hkv);
+  if (d != 128) return fail(ATTN_ERR_UNSUPPORTED, "FP8 head dim %d (128)", d);
+  if (!std::isfinite(scale)) return fail(ATTN_ERR_INVALID, "scale is not finite");
+  if (!(scale > 0.f)) return fail(ATTN_ERR_UNSUPPORTED, "scale must be > 0");
+  if (!window_ok(mask_kind, window))
+    return fail(ATTN_ERR_INVALID, "window %d out of range for mask_kind %d", window, mask_kind);
+  if (B == 0 || N == 0) return ATTN_OK;
+  if (!q8 || !k8 || !v || !o || !lse || !q_scales || !k_scales)
+    return fail(ATTN_ERR_INVALID, "null pointer");
+  if (!aligned16(q8) || !aligned16(k8) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return fail(ATTN_ERR_INVALID, "tensors must be 16-byte aligned");
+  if (static_cast<long long>(B) * Hq >= (1ll << 31))
+    return fail(ATTN_ERR_UNSUPPORTED, "B*Hq too large");
+  const long long units = static_cast<long long>(B) * Hq * pairs_for_rows(N);
+  if (units >= (1ll << 31) - 1) return fail(ATTN_ERR_UNSUPPORTED, "too many work units");
+  int* status = nullptr;
+  int rc = status_ptr(&status);
+  if (rc) return rc;
+  CUtensorMap tq, tk, tv, to;
+  if ((rc = encode_3d_u8(&tq, q8, d, N, static_cast<uint64_t>(B) * Hq, 128))) return rc;
+  if ((rc = encode_3d_u8(&tk, k8, d, N, static_cast<uint64_t>(B) * Hkv, 128))) return rc;
+  if ((rc = encode_3d(&tv, v, d, N, static_cast<uint64_t>(B) * Hkv, 128))) return rc;
+  if ((rc = encode_3d(&to, o, d, N, static_cast<uint64_t>(B) * Hq, 32))) return rc;
+  PrefillParams p{};
+  p.o = o;
+  p.lse = lse;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.N = N;
+  p.group = Hq / Hkv;
+  p.num_units = static_cast<int>(units);
+  p.window = window;
+  p.scale_log2 = scale * kLog2e;
+  p.q_scales = q_scales;
+  p.k_scales = k_scales;
+  p.nbq = p.nbk = (N + kFp8Block - 1) / kFp8Block;
+  p.status = status;
+  p.timeout_ns = kTimeoutNs;
+  int sms = 0;
+  if ((rc = sm_count(&sms))) return rc;
+  const int grid = p.num_units < sms ? p.num_units : sms;
+  cudaError_t e =
+      launch_prefill_fp8(mask_kind, tq, tk, tv, to, p, grid, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "FP8 prefill launch");
   return ATTN_OK;
 }
 

@@ -18,6 +18,11 @@ cudaError_t launch_prefill_d128(int mask, const CUtensorMap& q, const CUtensorMa
                                 const CUtensorMap& v, const CUtensorMap& o,
                                 const PrefillParams& p, int grid, cudaStream_t stream);
 
+// Launch prefill_kernel<128, mask, FP8 = true> (E4M3 Q / K; dense mask kinds).
+cudaError_t launch_prefill_fp8(int mask, const CUtensorMap& q, const CUtensorMap& k,
+                               const CUtensorMap& v, const CUtensorMap& o,
+                               const PrefillParams& p, int grid, cudaStream_t stream);
+
 // Launch decode_kernel<d, group> on grid (max_splits, Hkv, B).
 cudaError_t launch_decode(int d, int group, const CUtensorMap& k, const CUtensorMap& v,
                           const DecodeParams& p, dim3 grid, cudaStream_t stream);

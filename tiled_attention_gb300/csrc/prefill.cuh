@@ -37,6 +37,8 @@
 
 #include <cuda_bf16.h>
 
+#include <cfloat>
+
 #include "ptx.cuh"
 #include "sched.h"
 
@@ -53,6 +55,9 @@ struct PrefillParams {
   int num_units;            // work units; DOCUMENT: an upper bound (surplus ones decode invalid)
   int window;               // SLIDING / SLIDING_BIDIR window, PREFIX_LM prefix length
   float scale_log2;         // scale * log2(e)
+  const float* q_scales;    // FP8: [B*Hq, nbq] per-128-row-tile scales of Q
+  const float* k_scales;    // FP8: [B*Hkv, nbk] per-128-row-tile scales of K
+  int nbq, nbk;             // FP8: tiles per plane (ceil(N / 128))
   int* status;
   unsigned long long timeout_ns;
 };
@@ -245,7 +250,10 @@ __device__ __forceinline__ void exp2_pack_32(const float* f, float2 cc, float2 m
   }
 }
 
-template <int D, int MASK>
+// FP8: Q and K are E4M3 with one fp32 scale per 128-row tile (the block quantization of the
+// FlashAttention-3 page); S = Q K^T runs as tcgen05 kind::f8f6f4 and the two tile scales join
+// the softmax's per-tile constant. V, P and O stay bf16. Dense kinds, D = 128 only.
+template <int D, int MASK, bool FP8 = false>
 __global__ void __launch_bounds__(384, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
                    const __grid_constant__ CUtensorMap tm_k,
@@ -253,6 +261,15 @@ __global__ void __launch_bounds__(384, 1)
                    const __grid_constant__ CUtensorMap tm_o, const PrefillParams p) {
   using C = PrefillCfg<D>;
   constexpr int BM = C::BM, BN = C::BN, STAGES = C::kStages, QB = C::kQBufs;
+  static_assert(!FP8 || (D == 128 && !is_packed(MASK)), "FP8: dense kinds, D = 128");
+  // Q and K tiles: 64 bf16 or 128 E4M3 columns per 128-byte swizzle panel. Q buffers keep
+  // their bf16 size in both cases: the epilogue stages the bf16 O tile in them.
+  constexpr int kQKPanels = FP8 ? D / 128 : C::kPanels;
+  constexpr int kQKPanelCols = FP8 ? 128 : 64;
+  constexpr uint32_t kQLoadBytes = BM * D * (FP8 ? 1 : 2);
+  constexpr uint32_t kKLoadBytes = BN * D * (FP8 ? 1 : 2);
+  constexpr int kSSteps = FP8 ? D / 32 : D / 16;  // 32-byte K steps of one S = Q K^T
+  constexpr uint32_t kIdescS = FP8 ? idesc_e4m3(BM, BN) : C::kIdescS;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -342,10 +359,10 @@ __global__ void __launch_bounds__(384, 1)
             ok = mbar_wait(&ctl->q_empty[qb], ((qn / QB) & 1) ^ 1, wc);
             if (!ok) break;
             ++qn;
-            mbar_arrive_expect_tx(&ctl->q_full[qb], C::kQBytes);
-            for (int c = 0; c < C::kPanels; ++c)
+            mbar_arrive_expect_tx(&ctl->q_full[qb], kQLoadBytes);
+            for (int c = 0; c < kQKPanels; ++c)
               tma_load_3d(q_s + qb * C::kQBytes + c * C::kChunkBytes, &tm_q, &ctl->q_full[qb],
-                          c * 64, un.q_row0 + i * BM, un.bh);
+                          c * kQKPanelCols, un.q_row0 + i * BM, un.bh);
           }
           // PAGED_PREFILL: key tile j of the sequence is BN / P pages, each its own box of P
           // rows. The planes of a tile's pages are looked up once (all table reads issued
@@ -383,7 +400,7 @@ __global__ void __launch_bounds__(384, 1)
             const int st = e % STAGES;
             ok = mbar_wait(&ctl->kv_empty[st], ((e / STAGES) & 1) ^ 1, wc);
             if (!ok) break;
-            mbar_arrive_expect_tx(&ctl->kv_full[st], C::kKVBytes);
+            mbar_arrive_expect_tx(&ctl->kv_full[st], (x & 1) ? C::kKVBytes : kKLoadBytes);
             const CUtensorMap* m = (x & 1) ? &tm_v : &tm_k;
             uint8_t* dst = kv_s + st * C::kKVBytes;
             if (MASK == kMaskPagedPrefill) {
@@ -401,8 +418,10 @@ __global__ void __launch_bounds__(384, 1)
               }
               if (!(x & 1) && lo + x / 2 + 1 < hi) page_planes(lo + x / 2 + 1, pl_next);
             } else {
-              for (int c = 0; c < C::kPanels; ++c)
-                tma_load_3d(dst + c * C::kChunkBytes, m, &ctl->kv_full[st], c * 64,
+              const int npan = (x & 1) ? C::kPanels : kQKPanels;
+              const int pcols = (x & 1) ? 64 : kQKPanelCols;
+              for (int c = 0; c < npan; ++c)
+                tma_load_3d(dst + c * C::kChunkBytes, m, &ctl->kv_full[st], c * pcols,
                             un.k_org + (lo + x / 2) * BN, un.kvh);
             }
           }
@@ -488,11 +507,15 @@ __global__ void __launch_bounds__(384, 1)
               const uint32_t d_s = tmem + i * 128;
               const uint64_t q_desc = i ? q_desc1 : q_desc0;
 #pragma unroll
-              for (int kk = 0; kk < D / 16; ++kk) {
-                // K-major panels: a 16-column K step is 32 bytes inside a 128-byte swizzle
-                // row; every 4 steps move to the next 64-column panel. 8-row groups: 1024 B.
+              for (int kk = 0; kk < kSSteps; ++kk) {
+                // K-major panels: a K step (16 bf16 or 32 E4M3 columns) is 32 bytes inside a
+                // 128-byte swizzle row; every 4 steps move to the next panel. 8-row groups:
+                // 1024 B.
                 const uint32_t off16 = ((kk >> 2) * C::kChunkBytes + (kk & 3) * 32) >> 4;
-                mma_ss(d_s, q_desc + off16, k_desc + off16, C::kIdescS, kk > 0 ? 1u : 0u);
+                if constexpr (FP8)
+                  mma_ss_f8(d_s, q_desc + off16, k_desc + off16, kIdescS, kk > 0 ? 1u : 0u);
+                else
+                  mma_ss(d_s, q_desc + off16, k_desc + off16, kIdescS, kk > 0 ? 1u : 0u);
               }
               mma_commit(&ctl->s_ready[i]);
             }
@@ -520,7 +543,7 @@ __global__ void __launch_bounds__(384, 1)
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const uint32_t s_col = lane_base + i * 128;
     const uint32_t o_col = lane_base + 256 + i * D;
-    const float c = p.scale_log2;
+    const float c0 = p.scale_log2;
     int sc = 0, oc = 0;  // S tiles and finished units of this query tile consumed
     int qc = 0;          // Q loads of all tiles before this unit
     bool ok = true;
@@ -541,7 +564,18 @@ __global__ void __launch_bounds__(384, 1)
       const int row = q_row0 + i * BM + r;  // absolute query row
       float m_run = -INFINITY;  // running max in log2 units (may trail the true max by < 8)
       float l_run = 0.f;
+      // FP8: this query tile's scale; each key tile's joins it below.
+      const float cq = FP8 ? c0 * __ldg(p.q_scales + static_cast<size_t>(bh) * p.nbq +
+                                        (q_row0 + i * BM) / BM)
+                           : c0;
       for (int j = my.lo; j < my.hi && ok; ++j) {
+        // Scale of the raw scores in log2 units. FP8: times the key tile's scale, kept
+        // positive (a zero scale means an all-zero tile, whose raw scores are 0; a positive
+        // floor keeps masked -inf scores at -inf instead of NaN).
+        const float c =
+            FP8 ? fmaxf(cq * __ldg(p.k_scales + static_cast<size_t>(un.kvh) * p.nbk + j),
+                        FLT_MIN)
+                : c0;
         ok = __all_sync(0xffffffffu, mbar_wait(&ctl->s_ready[i], (sc++) & 1, wc));
         if (!ok) break;
         tc_fence_after();

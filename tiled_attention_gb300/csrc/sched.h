@@ -31,7 +31,7 @@ enum MaskKind { kMaskNone = 0, kMaskCausal = 1, kMaskSliding = 2, kMaskDocument 
 // (context length - chunk length). The chunk's last row then lines up with the context's
 // last key, and the causal rule j <= i of that shared index space is the chunked-prefill
 // mask: chunk row t sees the context's keys up to position (context - chunk) + t.
-TA_HD bool is_packed(int mask) {
+TA_HD constexpr bool is_packed(int mask) {
   return mask == kMaskDocument || mask == kMaskDocumentBidir || mask == kMaskPagedPrefill;
 }
 

@@ -37,6 +37,14 @@ class DeviceProblem:
                                                                  MASK_PAGED_PREFILL) else 0)
         self.seqlens_k = (None if w.seqlens_k is None else
                           torch.from_numpy(np.ascontiguousarray(w.seqlens_k, np.int32)).to(self.device))
+        self.fp8 = w.q8 is not None
+        if self.fp8:
+            self.q8 = torch.from_numpy(np.ascontiguousarray(w.q8)).to(self.device)
+            self.k8 = torch.from_numpy(np.ascontiguousarray(w.k8)).to(self.device)
+            self.q_scales = torch.from_numpy(np.ascontiguousarray(w.q_scales, np.float32)).to(
+                self.device)
+            self.k_scales = torch.from_numpy(np.ascontiguousarray(w.k_scales, np.float32)).to(
+                self.device)
         nbytes = (0 if w.mask_kind == MASK_PAGED_PREFILL else
                   attn.attn_workspace_bytes(w.B, w.Hq, w.Hkv, w.N, w.d, w.mask_kind, w.page_size))
         self.workspace = (torch.empty(max(nbytes, 16), dtype=torch.uint8, device=self.device)
@@ -44,6 +52,10 @@ class DeviceProblem:
 
     def run(self, stream=None) -> int:
         w = self.w
+        if self.fp8:
+            return attn.attn_fwd_fp8(self.q8, self.k8, self.v, self.o, self.lse, self.q_scales,
+                                     self.k_scales, w.B, w.Hq, w.Hkv, w.N, w.d, w.scale,
+                                     w.mask_kind, w.window, stream)
         if w.mask_kind == MASK_PAGED_PREFILL:
             return attn.attn_fwd_paged_prefill(self.q, self.k, self.v, self.o, self.lse, w.B,
                                                w.Hq, w.Hkv, w.N, w.d, w.scale, self.cu,
