@@ -483,40 +483,62 @@ def main():
             for t_name in ("o", "lse"):
                 d2h += host[name + t_name].numel() * host[name + t_name].element_size()
 
-        def e2e_step(evs):
-            evs[0].record(stream)
-            for t_name in ("q", "k", "v"):
-                getattr(pp, t_name).copy_(host["p" + t_name], non_blocking=True)
-            rc = pp.run(stream)
-            host["po"].copy_(pp.o, non_blocking=True)
-            host["plse"].copy_(pp.lse, non_blocking=True)
-            evs[1].record(stream)
-            for t_name in ("q", "k", "v", "cu", "table"):
-                getattr(pd, t_name).copy_(host["d" + t_name], non_blocking=True)
-            rc |= pd.run(stream)
-            host["do"].copy_(pd.o, non_blocking=True)
-            host["dlse"].copy_(pd.lse, non_blocking=True)
-            evs[2].record(stream)
-            return rc
+        # Each part runs as a pipeline over three streams (host -> device copies, compute,
+        # device -> host copies) with two device buffer sets, the way a serving loop feeds the
+        # library: step k+1's inputs upload while step k computes and step k-1's results
+        # download. Every step still copies its own inputs from pinned host memory and its O
+        # and LSE back; the time is taken with CUDA events from the first upload to the last
+        # download.
+        def e2e_part(name, dp_a, in_names, steps):
+            dps = [dp_a, DeviceProblem(dp_a.w, device=dev, fill_outputs=0.0)]
+            s_in, s_cp, s_out = (torch.cuda.Stream(dev) for _ in range(3))
+            n = steps + 2
+            ev_in = [torch.cuda.Event() for _ in range(n)]
+            ev_cp = [torch.cuda.Event() for _ in range(n)]
+            ev_out = [torch.cuda.Event() for _ in range(n)]
+            t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize(dev)
+            rc = 0
+            for k in range(n):
+                if k == 2:  # two untimed warm-up steps
+                    s_in.wait_event(ev_out[1])
+                    t0.record(s_in)
+                dp = dps[k % 2]
+                if k >= 2:
+                    s_in.wait_event(ev_cp[k - 2])  # this set's previous step has read its inputs
+                with torch.cuda.stream(s_in):
+                    for t_name in in_names:
+                        getattr(dp, t_name).copy_(host[name + t_name], non_blocking=True)
+                ev_in[k].record(s_in)
+                s_cp.wait_event(ev_in[k])
+                if k >= 2:
+                    s_cp.wait_event(ev_out[k - 2])  # and its previous results are downloaded
+                rc |= dp.run(s_cp)
+                ev_cp[k].record(s_cp)
+                s_out.wait_event(ev_cp[k])
+                with torch.cuda.stream(s_out):
+                    host[name + "o"].copy_(dp.o, non_blocking=True)
+                    host[name + "lse"].copy_(dp.lse, non_blocking=True)
+                ev_out[k].record(s_out)
+            t1.record(s_out)
+            torch.cuda.synchronize(dev)
+            assert rc == 0, attn.last_error()
+            del dps[1]
+            return t0.elapsed_time(t1)
 
-        eevs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)]
-                for _ in range(args.e2e_steps + 2)]
-        for k in range(2):
-            assert e2e_step(eevs[k]) == 0
-        torch.cuda.synchronize(dev)
-        for k in range(args.e2e_steps):
-            assert e2e_step(eevs[2 + k]) == 0
-        torch.cuda.synchronize(dev)
-        ep = sum(e[0].elapsed_time(e[1]) for e in eevs[2:])
-        ed = sum(e[1].elapsed_time(e[2]) for e in eevs[2:])
+        ep = e2e_part("p", pp, ("q", "k", "v"), args.e2e_steps)
+        ed = e2e_part("d", pd, ("q", "k", "v", "cu", "table"), args.e2e_steps)
+        assert attn.attn_get_status(stream) == 0
         ep, ed = max_over_ranks([ep, ed], dist, dev)
         e2e = {"value": replica_throughput(world, args.e2e_steps, flops, ep * 1e-3) / 1e12,
                "unit": "TFLOP/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "steps": args.e2e_steps,
                "decode_gbs": replica_throughput(world, args.e2e_steps, dec_bytes, ed * 1e-3) / 1e9,
-               "what": "pinned host -> device copies of the step's inputs, attn_fwd, device -> "
-                       "pinned host copies of O and LSE, per part of the step"}
+               "what": "per part of the step, pinned host -> device copies of its inputs, "
+                       "attn_fwd, device -> pinned host copies of O and LSE, pipelined over "
+                       "three streams with two device buffer sets; CUDA events from the first "
+                       "upload to the last download"}
 
     cpu = None
     if rank == 0 and world == 1 and args.cpu_budget > 0:
