@@ -172,13 +172,13 @@ __global__ void __launch_bounds__(160, 2)
 
   if (warp == C::kWarps) {
     // ---------------------------------------------------------------- TMA producer
-    if (lane == 0) {
-      prefetch_tensormap(&tm_k);
-      prefetch_tensormap(&tm_v);
-      const int* row = p.dense ? nullptr : p.table + static_cast<size_t>(b) * p.max_pages;
-      const int lp = p.page_shift;  // log2(page_size)
-      int issued = 0;
-      if (p.dense || lp >= 6) {
+    const int* row = p.dense ? nullptr : p.table + static_cast<size_t>(b) * p.max_pages;
+    const int lp = p.page_shift;  // log2(page_size)
+    int issued = 0;
+    if (p.dense || lp >= 6) {
+      if (lane == 0) {
+        prefetch_tensormap(&tm_k);
+        prefetch_tensormap(&tm_v);
         // One box per stage: 64 rows of the dense cache, or the whole (P = 64) or one half
         // (P = 128) of a page. A stage whose table entry is outside the pool (never addressed;
         // the status word reports it) is loaded from the plane just past the pool, which TMA
@@ -212,55 +212,54 @@ __global__ void __launch_bounds__(160, 2)
                         pn * 64, row0, plane);
           }
         }
-      } else {
-        // Pages of 16 or 32 tokens: stage k is 64 >> lp whole pages. Their planes are looked
-        // up one stage ahead (table reads issued together), so the lookup latency hides
-        // behind the current stage. A page past the context, or whose table entry is outside
-        // the pool, is loaded from the zero-filled plane past the pool.
-        const int nb = C::kPage >> lp;  // boxes per stage (4 or 2)
-        int pl[4], pl_next[4];
-        auto stage_planes = [&](int k, int (&out)[4]) {
-          int raw[4];
-#pragma unroll
-          for (int sb = 0; sb < 4; ++sb) {
-            const int tok = (pg0 + k) * C::kPage + (sb << lp);
-            raw[sb] = (sb < nb && tok < L) ? __ldg(row + (tok >> lp)) : -1;
-          }
-#pragma unroll
-          for (int sb = 0; sb < 4; ++sb) {
-            const int tok = (pg0 + k) * C::kPage + (sb << lp);
-            out[sb] = p.num_pages * p.Hkv;
-            if (sb < nb && tok < L) {
-              if (raw[sb] < 0 || raw[sb] >= p.num_pages)
-                report_status(p.status, -5);
-              else
-                out[sb] = raw[sb] * p.Hkv + g;
-            }
-          }
-        };
-        if (n > 0) stage_planes(0, pl_next);
-        for (int k = 0; k < n; ++k) {
-          const int st = k % S;
-          if (!mbar_wait(&ctl->empty[st], ((k / S) & 1) ^ 1, wc)) break;
-          ++issued;
-          uint8_t* dst = ring + st * C::kStageBytes;
-#pragma unroll
-          for (int sb = 0; sb < 4; ++sb) pl[sb] = pl_next[sb];
-          mbar_arrive_expect_tx(&ctl->full[st], C::kStageBytes);
-#pragma unroll
-          for (int sb = 0; sb < 4; ++sb) {
-            if (sb >= nb) break;
-#pragma unroll
-            for (int pn = 0; pn < C::kPanels; ++pn) {
-              tma_load_3d(dst + pn * C::kPanelBytes + (sb << lp) * 128, &tm_k, &ctl->full[st],
-                          pn * 64, 0, pl[sb]);
-              tma_load_3d(dst + C::kPageBytes + pn * C::kPanelBytes + (sb << lp) * 128, &tm_v,
-                          &ctl->full[st], pn * 64, 0, pl[sb]);
-            }
-          }
-          if (k + 1 < n) stage_planes(k + 1, pl_next);
-        }
       }
+    } else {
+      // Pages of 16 or 32 tokens: stage k is 64 >> lp whole pages, and lane sb < 64 >> lp
+      // owns page sb of every stage: it reads that page's table entry one stage ahead (so the
+      // read overlaps the current stage) and issues its boxes, in parallel with the other
+      // lanes. A page past the context, or whose table entry is outside the pool, is loaded
+      // from the zero-filled plane past the pool.
+      if (lane == 0) {
+        prefetch_tensormap(&tm_k);
+        prefetch_tensormap(&tm_v);
+      }
+      const int nb = C::kPage >> lp;  // boxes per stage (4 or 2)
+      auto plane_of = [&](int k) {
+        const int tok = (pg0 + k) * C::kPage + (lane << lp);
+        int pl = p.num_pages * p.Hkv;
+        if (lane < nb && tok < L) {
+          const int raw = __ldg(row + (tok >> lp));
+          if (raw < 0 || raw >= p.num_pages)
+            report_status(p.status, -5);
+          else
+            pl = raw * p.Hkv + g;
+        }
+        return pl;
+      };
+      int pl_next = n > 0 ? plane_of(0) : 0;
+      for (int k = 0; k < n; ++k) {
+        const int st = k % S;
+        bool okw = true;
+        if (lane == 0) okw = mbar_wait(&ctl->empty[st], ((k / S) & 1) ^ 1, wc);
+        if (!__shfl_sync(0xffffffffu, okw, 0)) break;
+        ++issued;
+        uint8_t* dst = ring + st * C::kStageBytes;
+        const int pl = pl_next;
+        if (lane == 0) mbar_arrive_expect_tx(&ctl->full[st], C::kStageBytes);
+        __syncwarp();
+        if (lane < nb) {
+#pragma unroll
+          for (int pn = 0; pn < C::kPanels; ++pn) {
+            tma_load_3d(dst + pn * C::kPanelBytes + (lane << lp) * 128, &tm_k, &ctl->full[st],
+                        pn * 64, 0, pl);
+            tma_load_3d(dst + C::kPageBytes + pn * C::kPanelBytes + (lane << lp) * 128, &tm_v,
+                        &ctl->full[st], pn * 64, 0, pl);
+          }
+        }
+        if (k + 1 < n) pl_next = plane_of(k + 1);
+      }
+    }
+    if (lane == 0) {
       for (int k = imax(0, issued - S); k < issued; ++k)
         mbar_wait(&ctl->full[k % S], (k / S) & 1, wc_drain);
     }

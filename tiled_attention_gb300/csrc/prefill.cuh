@@ -364,66 +364,64 @@ __global__ void __launch_bounds__(384, 1)
               tma_load_3d(q_s + qb * C::kQBytes + c * C::kChunkBytes, &tm_q, &ctl->q_full[qb],
                           c * kQKPanelCols, un.q_row0 + i * BM, un.bh);
           }
-          // PAGED_PREFILL: key tile j of the sequence is BN / P pages, each its own box of P
-          // rows. The planes of a tile's pages are looked up once (all table reads issued
-          // together) for its K and V, and the next tile's while this one's boxes go out. A
-          // page past the context, or whose table entry is outside the pool (never addressed;
-          // the status word reports it), is read from the plane just past the pool, which TMA
-          // fills with zeros, so the stage always receives its full bytes.
-          int pl[8], pl_next[8];
-          auto page_planes = [&](int j, int (&out)[8]) {
-            const int lp = p.page_shift;
-            const int nb = BN >> lp;
-            const int lk = un.k_end - un.k_org;
-            const int* trow = p.table + static_cast<size_t>(un.seq) * p.max_pages;
-            int raw[8];
-#pragma unroll
-            for (int sb = 0; sb < 8; ++sb) {
-              const int tok = j * BN + (sb << lp);
-              raw[sb] = (sb < nb && tok < lk) ? __ldg(trow + (tok >> lp)) : -1;
-            }
-#pragma unroll
-            for (int sb = 0; sb < 8; ++sb) {
-              const int tok = j * BN + (sb << lp);
-              out[sb] = p.num_pages * p.Hkv;
-              if (sb < nb && tok < lk) {
-                if (raw[sb] < 0 || raw[sb] >= p.num_pages)
-                  report_status(p.status, -5);
-                else
-                  out[sb] = raw[sb] * p.Hkv + un.kvh;
-              }
-            }
-          };
-          if (MASK == kMaskPagedPrefill && hi > lo) page_planes(lo, pl_next);
           // Ring entry e holds K_{lo + x/2} (x = e - first entry of the unit, even) or V.
-          for (int x = 0; x < 2 * (hi - lo) && ok; ++x, ++e) {
+          for (int x = 0; MASK != kMaskPagedPrefill && x < 2 * (hi - lo) && ok; ++x, ++e) {
             const int st = e % STAGES;
             ok = mbar_wait(&ctl->kv_empty[st], ((e / STAGES) & 1) ^ 1, wc);
             if (!ok) break;
             mbar_arrive_expect_tx(&ctl->kv_full[st], (x & 1) ? C::kKVBytes : kKLoadBytes);
             const CUtensorMap* m = (x & 1) ? &tm_v : &tm_k;
             uint8_t* dst = kv_s + st * C::kKVBytes;
-            if (MASK == kMaskPagedPrefill) {
-              const int lp = p.page_shift;
-              if (!(x & 1)) {
-#pragma unroll
-                for (int sb = 0; sb < 8; ++sb) pl[sb] = pl_next[sb];
-              }
-#pragma unroll
-              for (int sb = 0; sb < 8; ++sb) {
-                if (sb >= (BN >> lp)) break;
-                for (int c = 0; c < C::kPanels; ++c)
-                  tma_load_3d(dst + c * C::kChunkBytes + (sb << lp) * 128, m,
-                              &ctl->kv_full[st], c * 64, 0, pl[sb]);
-              }
-              if (!(x & 1) && lo + x / 2 + 1 < hi) page_planes(lo + x / 2 + 1, pl_next);
-            } else {
-              const int npan = (x & 1) ? C::kPanels : kQKPanels;
-              const int pcols = (x & 1) ? 64 : kQKPanelCols;
-              for (int c = 0; c < npan; ++c)
-                tma_load_3d(dst + c * C::kChunkBytes, m, &ctl->kv_full[st], c * pcols,
-                            un.k_org + (lo + x / 2) * BN, un.kvh);
+            const int npan = (x & 1) ? C::kPanels : kQKPanels;
+            const int pcols = (x & 1) ? 64 : kQKPanelCols;
+            for (int c = 0; c < npan; ++c)
+              tma_load_3d(dst + c * C::kChunkBytes, m, &ctl->kv_full[st], c * pcols,
+                          un.k_org + (lo + x / 2) * BN, un.kvh);
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (MASK == kMaskPagedPrefill) {
+          // Key tile j of the sequence is BN / P pages, each its own box of P rows, and lane
+          // sb < BN / P owns page sb of every tile: it reads that page's table entry (one tile
+          // ahead, so the read overlaps the current tile's copies) and issues its boxes; the
+          // table reads and the copies of a tile run in parallel across the lanes. A page past
+          // the context, or whose entry is outside the pool (never addressed; the status word
+          // reports it), is read from the plane just past the pool, which TMA fills with
+          // zeros, so the stage always receives its full bytes.
+          const int lp = p.page_shift;
+          const int nb = BN >> lp;
+          const int lk = un.k_end - un.k_org;
+          const int* trow = p.table + static_cast<size_t>(un.seq) * p.max_pages;
+          auto plane_of = [&](int j) {
+            const int tok = j * BN + (lane << lp);
+            int pl = p.num_pages * p.Hkv;
+            if (lane < nb && tok < lk) {
+              const int raw = __ldg(trow + (tok >> lp));
+              if (raw < 0 || raw >= p.num_pages)
+                report_status(p.status, -5);
+              else
+                pl = raw * p.Hkv + un.kvh;
             }
+            return pl;
+          };
+          int pl_next = hi > lo ? plane_of(lo) : 0;
+          int pl = 0;
+          for (int x = 0; x < 2 * (hi - lo) && ok; ++x, ++e) {
+            const int st = e % STAGES;
+            if (lane == 0) ok = mbar_wait(&ctl->kv_empty[st], ((e / STAGES) & 1) ^ 1, wc);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            if (lane == 0) mbar_arrive_expect_tx(&ctl->kv_full[st], C::kKVBytes);
+            __syncwarp();
+            const CUtensorMap* m = (x & 1) ? &tm_v : &tm_k;
+            uint8_t* dst = kv_s + st * C::kKVBytes;
+            if (!(x & 1)) pl = pl_next;
+            if (lane < nb) {
+              for (int c = 0; c < C::kPanels; ++c)
+                tma_load_3d(dst + c * C::kChunkBytes + (lane << lp) * 128, m, &ctl->kv_full[st],
+                            c * 64, 0, pl);
+            }
+            if (!(x & 1) && lo + x / 2 + 1 < hi) pl_next = plane_of(lo + x / 2 + 1);
           }
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
