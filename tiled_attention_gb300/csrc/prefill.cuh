@@ -543,6 +543,15 @@ __global__ void __launch_bounds__(384, 1)
     const uint32_t o_col = lane_base + 256 + i * D;
     const float c0 = p.scale_log2;
     int sc = 0, oc = 0;  // S tiles and finished units of this query tile consumed
+    int pending_q = -1;  // tile 1: Q buffer whose O store may still be reading it
+    auto release_pending = [&]() {
+      if (pending_q >= 0) {
+        if (lane == 0) bulk_wait_group_read0();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl->q_empty[pending_q]);
+        pending_q = -1;
+      }
+    };
     int qc = 0;          // Q loads of all tiles before this unit
     bool ok = true;
     for (int k = 0; ok; ++k) {
@@ -556,7 +565,10 @@ __global__ void __launch_bounds__(384, 1)
       const KvRange my = i ? rng[1] : rng[0];
       const int qn = qc + ((i == 1 && rng[0].hi > rng[0].lo) ? 1 : 0);  // this tile's Q load
       qc += (rng[0].hi > rng[0].lo ? 1 : 0) + (rng[1].hi > rng[1].lo ? 1 : 0);
-      if (my.hi <= my.lo) continue;
+      if (my.hi <= my.lo) {
+        release_pending();  // no key tile here to release it after
+        continue;
+      }
       const int q_row0 = un.q_row0, k_org = un.k_org, k_end = un.k_end, bh = un.bh;
       const int row_end = k_end;  // query rows and keys share one index space
       const int row = q_row0 + i * BM + r;  // absolute query row
@@ -656,6 +668,7 @@ __global__ void __launch_bounds__(384, 1)
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(&ctl->p_ready[i]);
+        release_pending();
       }
       if (!ok) break;
       // -------------------------------------------------------------- epilogue
@@ -707,16 +720,27 @@ __global__ void __launch_bounds__(384, 1)
             tma_store_3d(&tm_o, stage + cp * C::kChunkBytes + quarter * 32 * 128, cp * 64,
                          warp_row0, bh);
           bulk_commit_group();
-          // The buffer is handed back only after the stores have read it.
-          bulk_wait_group_read0();
         }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&ctl->q_empty[qn % QB]);
+      // The buffer goes back to the producer only after the stores have read it. Tile 0's
+      // buffer takes the next unit's tile-1 Q, so it is released now. Tile 1's takes a Q two
+      // units on: for the causal kinds it is released after this warp's next key tile (or at
+      // the end), so tile 1 starts its next unit without waiting for the store (measured: a
+      // gain for causal, causal-document and paged prefill, a loss for the two-sided window).
+      constexpr bool kDeferTile1 =
+          MASK == kMaskCausal || MASK == kMaskDocument || MASK == kMaskPagedPrefill;
+      if (i == 0 || !kDeferTile1) {
+        if (lane == 0) bulk_wait_group_read0();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl->q_empty[qn % QB]);
+      } else {
+        pending_q = qn % QB;
+      }
       if (live)
         p.lse[static_cast<size_t>(bh) * p.N + row] =
             l_run > 0.f ? (m_run + log2f(l_run)) * 0.69314718055994530942f : -INFINITY;
     }
+    release_pending();  // the last unit's store, before shared memory goes away
   }
 
   tc_fence_before();
