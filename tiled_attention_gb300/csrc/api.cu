@@ -246,13 +246,18 @@ __global__ void __launch_bounds__(256)
   const int r0 = t * kFp8Block;
   const int rows = imin(kFp8Block, N - r0);
   const size_t base = (static_cast<size_t>(pl) * N + r0) * d / 8;  // 8-element vectors
-  const int nvec = rows * d / 8;
+  const int nvec = rows * d / 8;  // at most 128 * 128 / 8 = 2048: 8 per thread
   __shared__ float red[8];
   __shared__ float s_scale;
+  // The block is read from global memory once and kept in registers for both passes.
+  constexpr int kPer = kFp8Block * 128 / 8 / 256;
+  uint4 v[kPer];
   float amax = 0.f;
-  for (int i = static_cast<int>(threadIdx.x); i < nvec; i += blockDim.x) {
-    const uint4 v = x[base + i];
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) {
+    const int idx = static_cast<int>(threadIdx.x) + k * 256;
+    v[k] = idx < nvec ? x[base + idx] : make_uint4(0u, 0u, 0u, 0u);
+    const uint32_t w[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
 #pragma unroll
     for (int e = 0; e < 4; ++e)
       amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(w[e])), fabsf(bf16_hi(w[e]))));
@@ -269,15 +274,17 @@ __global__ void __launch_bounds__(256)
   }
   __syncthreads();
   const float sc = s_scale;
-  for (int i = static_cast<int>(threadIdx.x); i < nvec; i += blockDim.x) {
-    const uint4 v = x[base + i];
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) {
+    const int idx = static_cast<int>(threadIdx.x) + k * 256;
+    if (idx >= nvec) break;
+    const uint32_t w[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
     uint32_t c[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e)
       c[e] = sc == 0.f ? 0u
                        : e4m3x2(__fdiv_rn(bf16_lo(w[e]), sc), __fdiv_rn(bf16_hi(w[e]), sc));
-    x8[base + i] = make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
+    x8[base + idx] = make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
   }
 }
 
