@@ -471,3 +471,51 @@ def test_side_stream():
     assert dp.run(stream=s) == 0
     s.synchronize()
     compare(w, dp)
+
+
+# ------------------------------------------------------------------ large and degenerate shapes
+
+def test_long_causal_sequence_sampled():
+    """One 32768-token causal sequence: 128 query-tile pairs of up to 256 key tiles each."""
+    w = I.dense_workload(1201, 1, 4, 1, 32768, 128, I.MASK_CAUSAL)
+    dp = run(w)
+    rng = np.random.default_rng(12)
+    n = int(np.prod(w.lse_shape))
+    heads = np.arange(w.Hq) * w.N
+    rows = np.unique(np.concatenate([rng.integers(0, n, 600), heads, heads + w.N - 1,
+                                     heads + 16383, heads + 16384]))
+    compare(w, dp, rows=rows)
+
+
+def test_many_units_per_sm():
+    """B=32, H=64 at N=512: 4096 work units, many rounds of the persistent grid."""
+    w = I.dense_workload(1202, 32, 64, 16, 512, 64, I.MASK_CAUSAL)
+    dp = run(w)
+    rng = np.random.default_rng(13)
+    rows = rng.integers(0, int(np.prod(w.lse_shape)), 3000)
+    compare(w, dp, rows=rows)
+
+
+def test_document_many_tiny_segments():
+    """2000 segments of 1-16 tokens: the unit list scans thousands of segments."""
+    rng = np.random.default_rng(14)
+    lens = rng.integers(1, 17, 2000)
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    w = I.document_workload(1203, int(cu[-1]), 4, 64, cu_seqlens=cu, Hkv=2)
+    compare(w, run(w), strict=False)
+
+
+def test_paged_decode_128k_context():
+    """A 131072-token context (128 splits of 1024 tokens) next to short ones."""
+    lens = [131072, 5, 4000]
+    w = I.paged_decode_workload(1204, len(lens), 0, 0, 8, 2, 128, context_lens=lens)
+    compare(w, run(w), strict=False)
+
+
+def test_paged_prefill_empty_chunks():
+    """Sequences whose chunk is empty contribute no rows and must not disturb the others."""
+    lk = [500, 64, 1000, 7]
+    lq = [0, 64, 0, 7]
+    w = I.paged_prefill_workload(1205, len(lk), 0, 0, 0, 0, 8, 2, 128, page_size=16,
+                                 context_lens=lk, chunk_lens=lq)
+    compare(w, run(w), strict=False)
