@@ -326,11 +326,10 @@ def test_units_paged_prefill_order_and_cover():
         attn.attn_plan_units(attn.ATTN_MASK_PAGED_PREFILL, 2, 1, 10, bad, np.array([5, 4]))
 
 
-@pytest.mark.parametrize("kind", [DOCUMENT, DOCUMENT_BIDIR])
-def test_units_document_order_and_cover(kind):
+def test_units_document_order_and_cover():
     cu = np.array([0, 5, 600, 601, 1400, 1400, 1700], dtype=np.int32)
     Hq = 2
-    u = attn.attn_plan_units(kind, len(cu) - 1, Hq, int(cu[-1]), cu)
+    u = attn.attn_plan_units(DOCUMENT, len(cu) - 1, Hq, int(cu[-1]), cu)
     want = [(s, h, t) for s in range(len(cu) - 1) for h in range(Hq)
             for t in range((int(cu[s + 1] - cu[s]) + 255) // 256)]
     assert sorted(u) == sorted(want)
@@ -340,3 +339,30 @@ def test_units_document_order_and_cover(kind):
     for t in set(levels):
         same = [(s, h) for s, h, tt in u if tt == t]
         assert same == sorted(same)
+
+
+def test_units_document_bidir_sorted_by_cost():
+    """Non-causal segments: every unit once, in decreasing cost (key tiles of its two query
+    tiles, from the scheduler's own ranges); equal costs by segment, pair, then head."""
+    cu = np.array([0, 5, 600, 601, 1400, 1400, 1700, 2000, 2129], dtype=np.int32)
+    Hq = 2
+    u = attn.attn_plan_units(DOCUMENT_BIDIR, len(cu) - 1, Hq, int(cu[-1]), cu)
+    want = [(s, h, t) for s in range(len(cu) - 1) for h in range(Hq)
+            for t in range((int(cu[s + 1] - cu[s]) + 255) // 256)]
+    assert sorted(u) == sorted(want)
+
+    def cost(s, t):
+        k0, k1 = int(cu[s]), int(cu[s + 1])
+        c = 0
+        for i in range(2):
+            r0 = k0 + 256 * t + 128 * i
+            if r0 < k1:
+                lo, hi = attn.attn_plan_kv_range(DOCUMENT_BIDIR, 0, r0, 128, k1, k0, k1, 128)
+                c += hi - lo
+        return c
+
+    keys = [(-cost(s, t), s, t, h) for s, h, t in u]
+    assert keys == sorted(keys)
+    # the 129-row segment: one pair of one tile plus a one-row tile, cost 2 + 2 = 4;
+    # the 300-row segment's last pair has one tile of three: cost 3
+    assert cost(7, 0) == 4 and cost(5, 1) == 3

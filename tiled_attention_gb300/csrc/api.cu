@@ -713,6 +713,25 @@ int attn_plan_units(int mask_kind, int B, int Hq, int N, const int32_t* cu, int3
     for (int level = npairs - 1; level >= 0; --level)
       for (int b = 0; b < B; ++b)
         for (int h = 0; h < Hq; ++h) units.insert(units.end(), {b, h, level});
+  } else if (mask_kind == ATTN_MASK_DOCUMENT_BIDIR) {
+    // Sorted by cost: levels are key-tile counts, highest first; on a level, segments in
+    // order, their pairs of that cost in order, then heads.
+    if (!cu) return ATTN_ERR_INVALID;
+    int cmax = 0;
+    for (int s = 0; s < B; ++s) {
+      const int len = cu[s + 1] - cu[s];
+      if (len < 0) return ATTN_ERR_SEQLENS;
+      cmax = imax(cmax, 2 * tiles_for_rows(len));
+    }
+    for (int c = cmax; c >= 1; --c)
+      for (int s = 0; s < B; ++s) {
+        const int len = cu[s + 1] - cu[s];
+        const int k = pairs_of_cost(len, c);
+        for (int x = 0; x < k; ++x) {
+          const int pair = 2 * tiles_for_rows(len) == c ? x : pairs_for_rows(len) - 1;
+          for (int h = 0; h < Hq; ++h) units.insert(units.end(), {s, h, pair});
+        }
+      }
   } else {
     if (!cu) return ATTN_ERR_INVALID;
     int tmax = 0;

@@ -120,8 +120,12 @@ struct UnitCursor {
 // Work unit u in launch order: levels from the deepest (most key tiles) down, then batch /
 // segment, then head (heads sharing a kv head are adjacent). The level of a unit is its pair
 // index inside its segment, plus, for PAGED_PREFILL, the pairs of context that precede the
-// chunk ((context - chunk) / 256), so long contexts start first. Units must be asked for in
-// increasing order with the same cursor; warp-collective.
+// chunk ((context - chunk) / 256), so long contexts start first. For DOCUMENT_BIDIR, where
+// every query row of a segment sees the whole segment, a unit costs 2 n key tiles (n = the
+// segment's tile count) or n (the last pair of an odd n, whose second tile is empty); its
+// level is that cost, a level holds every such pair of every segment (segment, then pair,
+// then head), and the list is sorted by cost. Units must be asked for in increasing order
+// with the same cursor; warp-collective.
 template <int MASK>
 __device__ __forceinline__ Unit decode_unit(int u, const PrefillParams& p, UnitCursor& cur) {
   Unit r{0, 0, 0, 0, 0, 0, 0};
@@ -142,6 +146,7 @@ __device__ __forceinline__ Unit decode_unit(int u, const PrefillParams& p, UnitC
   }
   // Packed kinds: the warp scans the segments 32 at a time.
   const int* cu = p.cu_seqlens;
+  constexpr bool kCostLevels = MASK == kMaskDocumentBidir;
   // First level of segment s.
   auto level0 = [&](int s) {
     return MASK == kMaskPagedPrefill ? (p.seqlens_k[s] - (cu[s + 1] - cu[s])) / kUnitRows : 0;
@@ -158,7 +163,9 @@ __device__ __forceinline__ Unit decode_unit(int u, const PrefillParams& p, UnitC
           const int lk = p.seqlens_k[s];
           bad |= lk < len || lk > p.max_pages * p.page_size;
         }
-        if (!bad) tmax = imax(tmax, level0(s) + pairs_for_rows(len));
+        if (!bad)
+          tmax = imax(tmax, kCostLevels ? 2 * tiles_for_rows(len) + 1
+                                        : level0(s) + pairs_for_rows(len));
       }
     }
     for (int off = 16; off; off >>= 1)
@@ -187,9 +194,13 @@ __device__ __forceinline__ Unit decode_unit(int u, const PrefillParams& p, UnitC
     for (int s0 = 0; s0 < p.B; s0 += 32) {
       const int s = s0 + lane;
       if (s < p.B) {
-        const int l0 = level0(s);
-        const int c = imin(cur.t - 1, l0 + pairs_for_rows(cu[s + 1] - cu[s]) - 1);
-        if (c >= l0) next = imax(next, c);
+        if (kCostLevels) {
+          next = imax(next, cost_below(cu[s + 1] - cu[s], cur.t));
+        } else {
+          const int l0 = level0(s);
+          const int c = imin(cur.t - 1, l0 + pairs_for_rows(cu[s + 1] - cu[s]) - 1);
+          if (c >= l0) next = imax(next, c);
+        }
       }
     }
     for (int off = 16; off; off >>= 1)
@@ -200,13 +211,54 @@ __device__ __forceinline__ Unit decode_unit(int u, const PrefillParams& p, UnitC
     if (next < 0) return r;
     for (int s0 = 0; s0 < p.B; s0 += 32) {
       const int s = s0 + lane;
-      cur.cnt += __popc(__ballot_sync(0xffffffffu, s < p.B && has_level(s, next)));
+      if (kCostLevels) {
+        int c = s < p.B ? pairs_of_cost(cu[s + 1] - cu[s], next) : 0;
+        for (int off = 16; off; off >>= 1) c += __shfl_xor_sync(0xffffffffu, c, off);
+        cur.cnt += c;
+      } else {
+        cur.cnt += __popc(__ballot_sync(0xffffffffu, s < p.B && has_level(s, next)));
+      }
     }
   }
   const int t = cur.t;
   const int idx = (u - cur.base) / p.Hq;
   const int h = (u - cur.base) % p.Hq;
   int seen = 0, seg = -1;
+  int pair = 0;
+  if (kCostLevels) {
+    // The idx-th pair on this cost level: an inclusive prefix sum of the segments' counts.
+    for (int s0 = 0; s0 < p.B && seg < 0; s0 += 32) {
+      const int s = s0 + lane;
+      const int len = s < p.B ? cu[s + 1] - cu[s] : 0;
+      const int c = s < p.B ? pairs_of_cost(len, t) : 0;
+      int incl = c;
+      for (int off = 1; off < 32; off <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += v;
+      }
+      const unsigned m = __ballot_sync(0xffffffffu, idx < seen + incl);
+      if (m) {
+        const int src = __ffs(m) - 1;
+        const int k = idx - seen - (__shfl_sync(0xffffffffu, incl, src) -
+                                    __shfl_sync(0xffffffffu, c, src));
+        seg = s0 + src;
+        // Pairs of the full cost come first; the odd last pair is on a level of its own.
+        pair = 2 * tiles_for_rows(cu[seg + 1] - cu[seg]) == t
+                   ? k
+                   : pairs_for_rows(cu[seg + 1] - cu[seg]) - 1;
+      }
+      seen += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (seg < 0) return r;
+    r.valid = 1;
+    r.bh = h;
+    r.kvh = h / p.group;
+    r.seq = seg;
+    r.k_end = cu[seg + 1];
+    r.q_row0 = cu[seg] + pair * kUnitRows;
+    r.k_org = cu[seg];
+    return r;
+  }
   for (int s0 = 0; s0 < p.B && seg < 0; s0 += 32) {
     const int s = s0 + lane;
     unsigned m = __ballot_sync(0xffffffffu, s < p.B && has_level(s, t));

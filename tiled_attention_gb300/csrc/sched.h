@@ -100,5 +100,22 @@ TA_HD int tile_kind(int mask, int window, int r0, int bm, int row_end, int k_org
 constexpr int kUnitRows = 256;
 
 TA_HD int pairs_for_rows(int rows) { return (rows + kUnitRows - 1) / kUnitRows; }
+// 128-row (query or key) tiles covering `rows` rows.
+TA_HD int tiles_for_rows(int rows) { return (rows + kUnitRows / 2 - 1) / (kUnitRows / 2); }
+// DOCUMENT_BIDIR work list: the pairs of a segment of `len` rows that cost c key tiles. Every
+// pair costs 2 n (n = tiles_for_rows(len)) except the last pair of an odd n, which costs n.
+TA_HD int pairs_of_cost(int len, int c) {
+  const int n = tiles_for_rows(len), np = pairs_for_rows(len);
+  const int full = (n & 1) ? np - 1 : np;
+  return (n > 0 && 2 * n == c ? full : 0) + ((n & 1) && n == c ? 1 : 0);
+}
+// The largest cost below `below` that a segment of `len` rows has pairs of; -1 if none.
+TA_HD int cost_below(int len, int below) {
+  const int n = tiles_for_rows(len), np = pairs_for_rows(len);
+  int c = -1;
+  if (n > 0 && ((n & 1) ? np - 1 : np) > 0 && 2 * n < below) c = 2 * n;
+  if ((n & 1) && n < below) c = imax(c, n);
+  return c;
+}
 
 }  // namespace ta
