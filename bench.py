@@ -206,6 +206,27 @@ def reference_arm(args, rank: int):
     print(json.dumps(line), flush=True)
 
 
+def measure_ex2_rate(attn, torch, dev, stream, iters=4096):
+    """Exp2 throughput ceiling of this GPU (exponentials per second): the library's MUFU probe
+    with eight resident 256-thread CTAs per SM, best of five timed launches after two."""
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    blocks = sms * 8
+    out = torch.empty(blocks * 256, dtype=torch.float32, device=dev)
+    for _ in range(2):
+        assert attn.attn_bench_ex2(out, blocks, iters, stream) == 0, attn.last_error()
+    best = 0.0
+    for _ in range(5):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        assert attn.attn_bench_ex2(out, blocks, iters, stream) == 0, attn.last_error()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        best = max(best, blocks * 256 * 8 * iters / (e0.elapsed_time(e1) * 1e-3))
+    assert bool(torch.isfinite(out).all())
+    return best
+
+
 def suite(args):
     """Time every specified workload and the mask variants one launch at a time (median of
     --steps launches after --warmup, L2 flushed before each launch by writing a 256 MB
@@ -464,6 +485,18 @@ def main():
         "algorithmic": f"valid-token K+V + q/o/lse/table bytes = {dec_bytes:.4e} B per launch",
     }
 
+    # ---- softmax exponentials against the measured exp2 ceiling
+    softmax_exp = None
+    if do_p:
+        ceiling = measure_ex2_rate(attn, torch, dev, stream)
+        n_exp = flops / (4 * wp.d)  # one exponential per visible (query, key) pair
+        softmax_exp = {
+            "achieved": n_exp / pre_avg_s, "ceiling": ceiling, "unit": "exp2/s",
+            "frac": n_exp / pre_avg_s / ceiling,
+            "algorithmic": f"B*Hq*sum(visible pairs) = {n_exp:.4e} exponentials per launch",
+            "ceiling_source": "attn_bench_ex2 on this GPU (ex2.approx, 8 CTAs x 256 threads "
+                              "per SM, 8 independent chains per thread), CUDA events"}
+
     # ---- end to end: host (pinned) buffers, copies inside the timed region
     e2e = None
     if args.e2e_steps > 0 and args.only is None:
@@ -564,6 +597,7 @@ def main():
                        "frac_hbm": decode_gbs / world / peaks["hbm_gbs"]},
             "roofline": roofline,
             "roofline_decode": roofline_decode,
+            "softmax_exp": softmax_exp,
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": launches_per_step * args.steps,

@@ -246,6 +246,15 @@ const char *attn_last_error(void);
  * Asynchronous; read the outcome with attn_get_status(stream). */
 int attn_selftest_wait_timeout(unsigned long long timeout_ns, void *stream);
 
+/* Measurement helper: the exp2 throughput ceiling of this GPU's special-function (MUFU) units,
+ * against which the softmax's exponentials per second are reported. Launches `blocks` CTAs of
+ * 256 threads (1 .. 65535); every thread evaluates `iters` (1 .. 2^20) rounds of eight
+ * independent chains x <- 2^(-x), with the same ex2.approx instruction the softmax uses, and
+ * writes one float per thread to `out` (device, blocks * 256 floats, caller-owned) so the work
+ * cannot be elided. Exponentials evaluated: blocks * 256 * 8 * iters. Asynchronous on
+ * `stream`; the caller times it. Returns ATTN_OK, ATTN_ERR_INVALID or ATTN_ERR_CUDA. */
+int attn_bench_ex2(float *out, int blocks, int iters, void *stream);
+
 /* Frees the library's cached device state (status word) on the current device. */
 void attn_release(void);
 

@@ -1,6 +1,7 @@
 """C-ABI library checks that need no GPU: it builds for sm_103a, loads, exports every symbol
 include/attn.h declares, rejects bad arguments before touching CUDA, and its tile scheduler is
 exact (checked exhaustively against the mask definitions on small tiles)."""
+import ctypes
 import itertools
 
 import numpy as np
@@ -366,3 +367,11 @@ def test_units_document_bidir_sorted_by_cost():
     # the 129-row segment: one pair of one tile plus a one-row tile, cost 2 + 2 = 4;
     # the 300-row segment's last pair has one tile of three: cost 3
     assert cost(7, 0) == 4 and cost(5, 1) == 3
+
+
+@pytest.mark.parametrize("blocks,iters", [(0, 10), (-1, 10), (70000, 10), (4, 0), (4, 1 << 21)])
+def test_bench_ex2_rejects_bad_arguments(blocks, iters):
+    """Argument checks run before any launch, so they need no GPU."""
+    fake = ctypes.c_void_p(256)  # never dereferenced: the call fails before launching
+    assert attn.lib().attn_bench_ex2(fake, blocks, iters, None) == attn.ATTN_ERR_INVALID
+    assert attn.lib().attn_bench_ex2(None, 4, 10, None) == attn.ATTN_ERR_INVALID

@@ -463,6 +463,19 @@ def test_bounded_wait_times_out_and_context_survives():
     compare(w, run(w))
 
 
+def test_exp2_probe_reaches_the_fixed_point():
+    """The exp2 throughput probe runs eight chains x <- 2^(-x) per thread; each converges to
+    the fixed point of 2^(-x) = x (0.6411857445...; the map contracts by ln2 * 0.64 = 0.44 per
+    round), so every stored value is 8 times it."""
+    blocks, iters = 4, 64
+    out = torch.full((blocks * 256,), float("nan"), dtype=torch.float32, device="cuda")
+    assert attn.attn_bench_ex2(out, blocks, iters) == 0
+    torch.cuda.synchronize()
+    x = 0.6411857445049859
+    assert abs(2.0 ** -x - x) < 1e-12
+    assert torch.allclose(out.cpu(), torch.full_like(out.cpu(), 8 * x), rtol=0, atol=2e-5)
+
+
 def test_side_stream():
     w = I.config(1)
     s = torch.cuda.Stream()

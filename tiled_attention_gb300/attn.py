@@ -59,6 +59,7 @@ _SIGS = {
     "attn_selftest_wait_timeout": (_i, [ctypes.c_ulonglong, _p]),
     "attn_paged_decode_noalloc": (_i, [_p, _p, _p, _p, _p, _i, _i, _i, _i, _i, ctypes.c_float,
                                        _p, _p, _i, _i, _p]),
+    "attn_bench_ex2": (_i, [_p, _i, _i, _p]),
 }
 
 
@@ -169,6 +170,11 @@ def attn_gather_pages(pool, dst, block_table, B, max_pages, Hkv, page_size, d, n
 
 def attn_selftest_wait_timeout(timeout_ns: int, stream=None) -> int:
     return lib().attn_selftest_wait_timeout(timeout_ns, _stream(stream))
+
+
+def attn_bench_ex2(out, blocks: int, iters: int, stream=None) -> int:
+    """Exp2 throughput probe; `out` is a float32 device tensor of blocks * 256 elements."""
+    return lib().attn_bench_ex2(_ptr(out), blocks, iters, _stream(stream))
 
 
 def attn_get_status(stream=None) -> int:

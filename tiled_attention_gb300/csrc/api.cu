@@ -306,6 +306,24 @@ __global__ void wait_timeout_selftest_kernel(unsigned long long timeout_ns, int*
   }
 }
 
+// Exp2 throughput probe: per thread, eight independent chains x <- 2^(-x), one ex2.approx
+// (the softmax's instruction) per chain and round. The chains settle at the fixed point of
+// 2^(-x) (about 0.641), so no value leaves (0, 1]. One float per thread is stored so the
+// work stays live.
+__global__ void ex2_rate_kernel(float* out, int iters) {
+  float x[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) x[k] = 0.1f * static_cast<float>(k) + 1e-3f * (threadIdx.x & 31);
+  for (int i = 0; i < iters; ++i) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) x[k] = fast_exp2(-x[k]);
+  }
+  float s = 0.f;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) s += x[k];
+  out[static_cast<size_t>(blockIdx.x) * 256 + threadIdx.x] = s;
+}
+
 }  // namespace ta
 
 using namespace ta;
@@ -323,6 +341,16 @@ int attn_selftest_wait_timeout(unsigned long long timeout_ns, void* stream) {
                                                                                status);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "self-test launch");
+  return ATTN_OK;
+}
+
+int attn_bench_ex2(float* out, int blocks, int iters, void* stream) {
+  g_last_error.clear();
+  if (!out || blocks < 1 || blocks > 65535 || iters < 1 || iters > (1 << 20))
+    return fail(ATTN_ERR_INVALID, "attn_bench_ex2: out, blocks in [1, 65535], iters in [1, 2^20]");
+  ex2_rate_kernel<<<blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(out, iters);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "ex2 rate launch");
   return ATTN_OK;
 }
 
