@@ -170,8 +170,13 @@ def test_fp8_validation_before_cuda():
 def test_workspace_bytes():
     assert attn.attn_workspace_bytes(4, 16, 16, 2048, 128, CAUSAL, 0) == 0
     n = attn.attn_workspace_bytes(32, 32, 8, 16384, 128, 4, 64)
-    # partial O for 16 splits x 4 heads x 128 columns per (sequence, kv head), plus stats
-    assert n >= 32 * 8 * 16 * 4 * 128 * 4
+    # 256 (sequence, kv head) groups, at least one per SM: splits of 32 stages of 64 tokens,
+    # 8 splits of a 16384-token context. Partial O for 8 splits x 4 heads x 128 columns per
+    # group, plus stats and tickets.
+    assert 32 * 8 * 8 * 4 * 128 * 4 <= n < 32 * 8 * 8 * 4 * 130 * 4 + 4096
+    # fewer groups than SMs: 1 sequence x 8 kv heads, splits of 16 stages (16 splits)
+    m = attn.attn_workspace_bytes(1, 32, 8, 16384, 128, 4, 64)
+    assert 8 * 16 * 4 * 128 * 4 <= m < 8 * 16 * 4 * 130 * 4 + 4096
     # the dense-cache decode splits the same way and ignores page_size
     assert attn.attn_workspace_bytes(32, 32, 8, 16384, 128, attn.ATTN_MASK_DECODE, 0) == n
 
