@@ -532,3 +532,59 @@ def test_paged_prefill_empty_chunks():
     w = I.paged_prefill_workload(1205, len(lk), 0, 0, 0, 0, 8, 2, 128, page_size=16,
                                  context_lens=lk, chunk_lens=lq)
     compare(w, run(w), strict=False)
+
+
+# ------------------------------------------------------------------ randomized shapes
+
+_FUZZ_KINDS = [I.MASK_NONE, I.MASK_CAUSAL, I.MASK_SLIDING, I.MASK_SLIDING_BIDIR, I.MASK_PREFIX_LM,
+               I.MASK_DOCUMENT, I.MASK_DOCUMENT_BIDIR, I.MASK_PAGED_DECODE, I.MASK_DECODE,
+               I.MASK_PAGED_PREFILL]
+
+
+def _fuzz_workload(idx):
+    """Case idx: its mask kind in turn, the rest drawn from a generator seeded by idx: head dim,
+    batch, GQA group (any divisor for prefill, 3 included; 1/2/4/8 for decode), lengths,
+    windows and prefixes past the sequence, empty segments and chunks, page sizes."""
+    rng = np.random.default_rng(5000 + idx)
+    kind = _FUZZ_KINDS[idx % len(_FUZZ_KINDS)]
+    d = int(rng.choice([64, 128]))
+    Hkv = int(rng.integers(1, 4))
+    decode = kind in (I.MASK_PAGED_DECODE, I.MASK_DECODE)
+    Hq = Hkv * int(rng.choice([1, 2, 4, 8]) if decode else rng.integers(1, 5))
+    seed = 6000 + idx
+    if kind in (I.MASK_DOCUMENT, I.MASK_DOCUMENT_BIDIR):
+        lens = rng.integers(0, 400, int(rng.integers(1, 7)))
+        lens[int(rng.integers(0, len(lens)))] += 1  # at least one row
+        cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+        return I.document_workload(seed, int(cu[-1]), Hq, d, cu_seqlens=cu, Hkv=Hkv,
+                                   mask_kind=kind, name=f"fuzz{idx}")
+    B = int(rng.integers(1, 5))
+    page = int(rng.choice([16, 32, 64, 128]))
+    if kind == I.MASK_PAGED_DECODE:
+        return I.paged_decode_workload(seed, B, 0, 0, Hq, Hkv, d, page_size=page,
+                                       context_lens=rng.integers(1, 3000, B), name=f"fuzz{idx}")
+    if kind == I.MASK_DECODE:
+        lens = rng.integers(1, 2000, B)
+        return I.dense_decode_workload(seed, B, 0, 0, Hq, Hkv, d,
+                                       N=int(lens.max() + rng.integers(0, 100)),
+                                       context_lens=lens, name=f"fuzz{idx}")
+    if kind == I.MASK_PAGED_PREFILL:
+        lk = rng.integers(1, 2000, B)
+        lq = np.array([int(rng.integers(0, n + 1)) for n in lk])
+        lq[int(rng.integers(0, B))] = max(int(lq.max()), 1)
+        lq = np.minimum(lq, lk)
+        return I.paged_prefill_workload(seed, B, 0, 0, 0, 0, Hq, Hkv, d, page_size=page,
+                                        context_lens=lk, chunk_lens=lq, name=f"fuzz{idx}")
+    N = int(rng.integers(1, 700))
+    window = 0
+    if kind == I.MASK_SLIDING:
+        window = int(rng.integers(1, N + 130))
+    elif kind in (I.MASK_SLIDING_BIDIR, I.MASK_PREFIX_LM):
+        window = int(rng.integers(0, N + 130))
+    return I.dense_workload(seed, B, Hq, Hkv, N, d, kind, window, name=f"fuzz{idx}")
+
+
+@pytest.mark.parametrize("idx", range(40))
+def test_randomized_shapes(idx):
+    w = _fuzz_workload(idx)
+    compare(w, run(w), strict=False)
