@@ -488,21 +488,62 @@ __global__ void __launch_bounds__(160, 2)
   named_barrier_sync(1, C::kConsumers);
   if (!ctl->is_last) return;
   __threadfence();
-  // Last split of (b, g): merge the splits in split order.
-  for (int idx = tid; idx < G * D; idx += C::kConsumers) {
-    const int hh = idx / D, d = idx % D;
-    const size_t base0 = (bg * p.max_splits) * G + hh;
-    float M = -INFINITY;
-    for (int s = 0; s < nsplit; ++s) M = fmaxf(M, __ldcg(p.part_ml + 2 * (base0 + s * G)));
-    float Ls = 0.f, Os = 0.f;
-    for (int s = 0; s < nsplit; ++s) {
-      const size_t bs = base0 + static_cast<size_t>(s) * G;
-      const float w = exp2f(__ldcg(p.part_ml + 2 * bs) - M);
-      Ls += __ldcg(p.part_ml + 2 * bs + 1) * w;
-      Os += __ldcg(p.part_o + bs * D + d) * w;
+  // Last split of (b, g): merge the splits in split order. Every split's (m, l) is read once
+  // into shared memory (the ring is idle now) and turned into its weight 2^(m - M); each
+  // output element then sums its splits from independent loads, in split order, so the
+  // result is the same as a plain loop over the splits.
+  const size_t base_bg = bg * p.max_splits * G;  // (b, g)'s first partial row
+  constexpr int kMergeCap = C::kRingBytes / (8 * G);  // splits whose (w, l) fit the ring
+  if (nsplit <= kMergeCap) {
+    float* sw = reinterpret_cast<float*>(ring);  // [G][nsplit]: m, then the weight
+    float* sl = sw + G * nsplit;                 // [G][nsplit]: l
+    for (int hh = warp; hh < G; hh += C::kWarps) {
+      float M = -INFINITY;
+      for (int s = lane; s < nsplit; s += 32) {
+        const size_t bs = base_bg + static_cast<size_t>(s) * G + hh;
+        const float m = __ldcg(p.part_ml + 2 * bs);
+        sw[hh * nsplit + s] = m;
+        sl[hh * nsplit + s] = __ldcg(p.part_ml + 2 * bs + 1);
+        M = fmaxf(M, m);
+      }
+      for (int off = 16; off; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+      for (int s = lane; s < nsplit; s += 32) sw[hh * nsplit + s] = exp2f(sw[hh * nsplit + s] - M);
+      if (lane == 0) red_m[hh] = M;
     }
-    o16[(head0 + hh) * D + d] = bf16_bits(Os / Ls);
-    if (d == 0) p.lse[head0 + hh] = (M + log2f(Ls)) * 0.69314718055994530942f;
+    named_barrier_sync(1, C::kConsumers);
+    if (tid < G) {
+      float Ls = 0.f;
+      for (int s = 0; s < nsplit; ++s) Ls += sl[tid * nsplit + s] * sw[tid * nsplit + s];
+      red_l[tid] = Ls;
+    }
+    named_barrier_sync(1, C::kConsumers);
+    for (int idx = tid; idx < G * D; idx += C::kConsumers) {
+      const int hh = idx / D, d = idx % D;
+      const float* wv = sw + hh * nsplit;
+      const float* po = p.part_o + (base_bg + hh) * D + d;
+      float Os = 0.f;
+#pragma unroll 4
+      for (int s = 0; s < nsplit; ++s) Os += __ldcg(po + static_cast<size_t>(s) * G * D) * wv[s];
+      const float Ls = red_l[hh];
+      o16[(head0 + hh) * D + d] = bf16_bits(Os / Ls);
+      if (d == 0) p.lse[head0 + hh] = (red_m[hh] + log2f(Ls)) * 0.69314718055994530942f;
+    }
+  } else {
+    for (int idx = tid; idx < G * D; idx += C::kConsumers) {
+      const int hh = idx / D, d = idx % D;
+      const size_t base0 = base_bg + hh;
+      float M = -INFINITY;
+      for (int s = 0; s < nsplit; ++s) M = fmaxf(M, __ldcg(p.part_ml + 2 * (base0 + s * G)));
+      float Ls = 0.f, Os = 0.f;
+      for (int s = 0; s < nsplit; ++s) {
+        const size_t bs = base0 + static_cast<size_t>(s) * G;
+        const float w = exp2f(__ldcg(p.part_ml + 2 * bs) - M);
+        Ls += __ldcg(p.part_ml + 2 * bs + 1) * w;
+        Os += __ldcg(p.part_o + bs * D + d) * w;
+      }
+      o16[(head0 + hh) * D + d] = bf16_bits(Os / Ls);
+      if (d == 0) p.lse[head0 + hh] = (M + log2f(Ls)) * 0.69314718055994530942f;
+    }
   }
   if (tid == 0) p.counters[bg] = 0;
 }
