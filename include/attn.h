@@ -18,6 +18,10 @@
  *  - Conditions only the device can see (a bad cu_seqlens entry, a block-table entry outside
  *    the pool, a pipeline wait that ran past its time limit) are written to a device status
  *    word that attn_get_status() reads and clears.
+ *  - CUDA graphs: the first call on a device sets one-time kernel attributes and caches device
+ *    addresses. From then on every compute entry point only enqueues memsets and kernel
+ *    launches on the given stream, so it may be captured into a CUDA graph and replayed with
+ *    new inputs written in place (attn_get_status(), which synchronises, may not be captured).
  */
 #ifndef TILED_ATTN_H
 #define TILED_ATTN_H

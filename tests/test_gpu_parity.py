@@ -15,7 +15,7 @@ import torch
 import oracle
 from tiled_attention_gb300 import attn
 from tiled_attention_gb300 import inputs as I
-from tiled_attention_gb300.runner import DeviceProblem
+from tiled_attention_gb300.runner import DeviceProblem, bf16_tensor
 
 pytestmark = pytest.mark.gpu
 
@@ -588,3 +588,35 @@ def _fuzz_workload(idx):
 def test_randomized_shapes(idx):
     w = _fuzz_workload(idx)
     compare(w, run(w), strict=False)
+
+
+# ------------------------------------------------------------------ CUDA graphs
+
+def test_cuda_graph_capture_and_replay():
+    """After one ordinary call (which sets the one-time kernel attributes and caches), every
+    entry point enqueues only memsets and kernel launches on the caller's stream, so a causal
+    prefill and a paged decode can be captured into one CUDA graph. Replaying it on new
+    inputs, written in place into the captured buffers, gives the oracle's results for those
+    inputs."""
+    wp = I.dense_workload(71, 2, 4, 2, 300, 128, I.MASK_CAUSAL)
+    wd = I.paged_decode_workload(72, 3, 100, 2000, 8, 2, 128)
+    pp, pd = DeviceProblem(wp), DeviceProblem(wd)
+    assert pp.run() == 0 and pd.run() == 0, attn.last_error()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        rc = pp.run() | pd.run()
+    assert rc == 0, attn.last_error()
+    # new query, key and value values for the prefill, new queries for the decode
+    wp2 = I.dense_workload(73, 2, 4, 2, 300, 128, I.MASK_CAUSAL)
+    wd2 = I.paged_decode_workload(72, 3, 100, 2000, 8, 2, 128)
+    wd2.q = I.dense_workload(74, 3, 8, 2, 1, 128).q
+    for dst, src in ((pp.q, wp2.q), (pp.k, wp2.k), (pp.v, wp2.v), (pd.q, wd2.q)):
+        dst.copy_(bf16_tensor(src, dst.device).reshape(dst.shape))
+    for t in (pp.o, pd.o):
+        t.fill_(float("nan"))
+    g.replay()
+    torch.cuda.synchronize()
+    assert attn.attn_get_status() == 0
+    compare(wp2, pp, strict=False)
+    compare(wd2, pd)
