@@ -162,6 +162,14 @@ def cpu_baseline_sample(w, budget_s: float, seed: int, threads: int = 0):
     return n, row_flops(rows), dt
 
 
+def step_config(world: int):
+    """The workload description both arms report (the step: prefill, then paged decode)."""
+    return {"workload": f"prefill {PREFILL_NAME} + {DECODE_NAME}",
+            "prefill": PREFILL_NAME, "decode": DECODE_NAME,
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+            "l2": "inputs larger than L2 (335 MB prefill, 1.3 GB decode), no flush"}
+
+
 def reference_arm(args, rank: int):
     """The oracle (plain fp64 CPU) timed on the host cores: each step a bounded row sample."""
     if rank != 0:
@@ -195,8 +203,7 @@ def reference_arm(args, rank: int):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": t_total / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": PREFILL_NAME, "sample": f"{rows_per_step} random query rows "
-                   "per step", "l2": "n/a (CPU)"},
+        "config": step_config(args.gpus),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                          "sample": f"{rows_per_step} random query rows of {PREFILL_NAME} per "
                                    "step, fp64, materialised scores"},
@@ -588,10 +595,7 @@ def main():
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",
-            "config": {"workload": f"prefill {PREFILL_NAME} + {DECODE_NAME}",
-                       "prefill": PREFILL_NAME, "decode": DECODE_NAME,
-                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                       "l2": "inputs larger than L2 (335 MB prefill, 1.3 GB decode), no flush"},
+            "config": step_config(world),
             "prefill_frac_bf16_peak": prefill_tflops / world / peaks["bf16_tflops"],
             "decode": {"value": decode_gbs, "unit": "GB/s",
                        "frac_hbm": decode_gbs / world / peaks["hbm_gbs"]},
