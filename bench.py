@@ -251,6 +251,7 @@ def suite(args):
     peaks = load_peaks()
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     tag = "of " + peaks["source"]
+    ex2_ceiling = measure_ex2_rate(attn, torch, dev, stream)
 
     def timed(fn, reps):
         times = []
@@ -282,8 +283,10 @@ def suite(args):
                         peak=f"HBM copy {tag}")
         else:
             tf = w.flops() / (ms * 1e-3) / 1e12
+            exps = w.flops() / (4 * w.d) / (ms * 1e-3)  # one exponential per visible pair
             line.update(value=tf, unit="TFLOP/s", frac=tf / peaks["bf16_tflops"],
-                        peak=f"bf16 burst {tag}", flops=w.flops())
+                        peak=f"bf16 burst {tag}", flops=w.flops(), exp2_per_s=exps,
+                        exp2_frac_of_ceiling=exps / ex2_ceiling)
         if extra:
             line.update(extra)
         print(json.dumps(line), flush=True)
