@@ -10,8 +10,9 @@
 // per-sequence caches [B, Hkv, L, D] (p.dense): the second stage of that page's two-stage
 // path, which first gathers the pages into such a cache.
 //
-// Grid (split, kv head g, sequence b): a CTA handles `chunk_pages` 64-token stages of one (b, g) for
-// all G = Hq/Hkv query heads of the group. Decode reads each K/V byte once and is HBM-bound;
+// Grid (split, kv head g, sequence b): a CTA handles `chunk_pages` 64-token stages of one
+// (b, g) (32 when the batch has at least as many (b, g) groups as SMs, else 16; the host
+// chooses) for all G = Hq/Hkv query heads of the group. Decode reads each K/V byte once and is HBM-bound;
 // the arithmetic only has to stay off the critical path. It runs as warp-level bf16 MMAs
 // (mma.sync m16n8k16, fp32 accumulate) with the G heads as the rows of a 16-row tile: an
 // instruction-count choice, not a throughput one (scalar FMAs needed ~600 instructions per
@@ -22,7 +23,8 @@
 // partial results are merged once per chunk with the same rescaling identity.
 //
 // Combine: each split writes its unnormalised O, max m and sum l (log2 units) to the
-// workspace; the last split to finish (atomic ticket per (b, g)) merges them in split order:
+// workspace; the last split to finish (atomic ticket per (b, g)) merges them in split order,
+// reading each split's (m, l) once into shared memory:
 //   M = max_c m_c,  L = sum_c l_c 2^(m_c - M),  O = sum_c O_c 2^(m_c - M) / L,
 //   LSE = (M + log2 L) ln 2
 // — the same rescaling identity as the online update, applied across splits. The order is

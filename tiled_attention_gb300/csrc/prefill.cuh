@@ -4,9 +4,12 @@
 //
 // Work unit: two 128-row query tiles of one (batch or segment, query head). The kernel is
 // persistent, one CTA per SM: CTA b of G takes units b, 2G-1-b, 2G+b, 4G-1-b, ... of the
-// longest-first unit list (a snake over rounds, which evens out the per-SM sums). The K/V ring,
-// three rotating Q buffers and every barrier phase run on across units, so the next unit's
-// loads and first S MMAs overlap the current unit's last tiles and epilogue.
+// longest-first unit list (a snake over rounds, which evens out the per-SM sums; the list is
+// ordered by pair level, or by unit cost for non-causal documents: see decode_unit). The K/V
+// ring, three rotating Q buffers and every barrier phase run on across units, so the next
+// unit's loads and first S MMAs overlap the current unit's last tiles and epilogue. Within a
+// unit the key tiles are visited in ascending order; at d = 64 tile 1's extra tiles come first
+// (kRot, see geometry).
 //
 // The tiled computation with a running row max m and row sum l, rescaling the output
 // accumulator by exp(m - m_new) when the max grows, is the one described in "Flash MSA
