@@ -252,6 +252,7 @@ def suite(args):
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     tag = "of " + peaks["source"]
     ex2_ceiling = measure_ex2_rate(attn, torch, dev, stream)
+    wanted = None if not args.workloads else set(args.workloads.split(","))
 
     def timed(fn, reps):
         times = []
@@ -292,6 +293,8 @@ def suite(args):
         print(json.dumps(line), flush=True)
 
     for cfg in (1, 2, 3, "3c", 4, "3b", "3p", "4b", "6", "6p64", 5, "5p16"):
+        if wanted is not None and str(cfg) not in wanted:
+            continue
         w = I.config(cfg)
         dp = DeviceProblem(w, device=dev, fill_outputs=0.0)
         emit(w, timed(lambda: dp.run(stream), args.steps))
@@ -383,6 +386,8 @@ def main():
                     help="time one part of the step only (for profiler captures)")
     ap.add_argument("--suite", action="store_true",
                     help="time every workload one launch at a time (one JSON line each)")
+    ap.add_argument("--workloads", default=None,
+                    help="with --suite: comma-separated workload keys to time (e.g. 4,4b)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.suite:
