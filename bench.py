@@ -71,21 +71,23 @@ def recorded_traffic(kernel: str, sources):
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle sampling while the timed region runs."""
+    """nvidia-smi clock / power / throttle sampling while a timed region runs."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,"
+              "utilization.gpu")
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, period_ms: int = 100):
         self.gpu = gpu_index
+        self.period_ms = period_ms
         self.proc = None
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", str(self.period_ms)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
@@ -103,24 +105,40 @@ class ClockSampler:
                 self.proc.kill()
                 self.out, _ = self.proc.communicate()
 
-    def summary(self):
+    def rows(self):
+        """(sm MHz, max sm MHz, power W, [reason flags], utilization %) per sample."""
         rows = []
         for line in (self.out or "").strip().splitlines():
             parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 9:
+            if len(parts) < 10:
                 continue
             try:
-                rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+                util = float(parts[9]) if parts[9] not in ("", "[N/A]") else 0.0
+                power = float(parts[3]) if parts[3] not in ("", "[N/A]") else float("nan")
+                rows.append((float(parts[1]), float(parts[2]), power, parts[5:9], util))
             except ValueError:
                 continue
+        return rows
+
+    def summary(self):
+        rows = self.rows()
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for _, _, r in rows for i, v in enumerate(r)
+        reasons = sorted({names[i] for _, _, _, r, _ in rows for i, v in enumerate(r)
                           if v.lower() == "active"})
-        loaded = [c for c, _, _ in rows]
-        return {"sm_mhz": float(np.median(loaded)), "sm_max_mhz": rows[0][1],
-                "reasons": reasons, "samples": len(rows)}
+        # Samples taken while the GPU was busy; the region may be shorter than one period,
+        # in which case every sample is kept and the clock is the idle one.
+        loaded = [r for r in rows if r[4] >= 50.0]
+        use = loaded or rows
+        out = {"sm_mhz": float(np.median([r[0] for r in use])), "sm_max_mhz": rows[0][1],
+               "reasons": reasons, "samples": len(rows), "samples_under_load": len(loaded),
+               "period_ms": self.period_ms}
+        pw = [r[2] for r in use if np.isfinite(r[2])]
+        if pw:
+            out["power_w_median"] = float(np.median(pw))
+            out["power_w_max"] = float(np.max(pw))
+        return out
 
 
 def max_over_ranks(values, dist=None, device="cpu"):
@@ -380,6 +398,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="own", choices=["own", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--sustain-s", type=float, default=3.0,
+                    help="seconds of back-to-back steps after the timed region, with the clocks "
+                         "sampled under load (0 to skip)")
     ap.add_argument("--cpu-budget", type=float, default=12.0,
                     help="seconds of oracle work for the CPU baseline (rank 0, N=1 only)")
     ap.add_argument("--only", choices=["prefill", "decode"], default=None,
@@ -451,7 +472,7 @@ def main():
     if dist:
         dist.barrier()
     torch.cuda.synchronize(dev)
-    with ClockSampler(dev.index) as clk:
+    with ClockSampler(dev.index, period_ms=20) as clk:
         t_start = torch.cuda.Event(enable_timing=True)
         t_end = torch.cuda.Event(enable_timing=True)
         t_start.record(stream)
@@ -588,6 +609,49 @@ def main():
                        "three streams with two device buffer sets; CUDA events from the first "
                        "upload to the last download"}
 
+    # ---- sustained: the same step back to back for a few seconds, outside the timed steps,
+    # with the clocks sampled under load (a long-running job settles at a lower SM clock
+    # under the power cap than the short timed region above)
+    sustained = None
+    if args.sustain_s > 0 and args.only is None:
+        chunk = 64
+        t_wall = 0.0
+        pre_s = dec_s = 0.0
+        n_steps = 0
+        torch.cuda.synchronize(dev)
+        with ClockSampler(dev.index, period_ms=50) as sclk:
+            w0 = time.perf_counter()
+            while t_wall < args.sustain_s:
+                cev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)]
+                       for _ in range(chunk)]
+                for k in range(chunk):
+                    assert step(cev[k]) == 0, attn.last_error()
+                torch.cuda.synchronize(dev)
+                pre_s += sum(e[0].elapsed_time(e[1]) for e in cev) * 1e-3
+                dec_s += sum(e[1].elapsed_time(e[2]) for e in cev) * 1e-3
+                n_steps += chunk
+                t_wall = time.perf_counter() - w0
+        assert attn.attn_get_status(stream) == 0
+        pre_s, dec_s = max_over_ranks([pre_s, dec_s], dist, dev)
+        sc = sclk.summary()
+        s_tf = replica_throughput(world, n_steps, flops, pre_s) / 1e12
+        s_gbs = replica_throughput(world, n_steps, dec_bytes, dec_s) / 1e9
+        mhz = sc.get("sm_mhz")
+        sustained = {
+            "seconds": t_wall, "steps": n_steps,
+            "prefill_tflops": s_tf,
+            "prefill_frac_of_sustained_peak": s_tf / world / peaks["bf16_tflops_sustained"],
+            "prefill_frac_of_burst_peak": s_tf / world / peaks["bf16_tflops"],
+            "decode_gbs": s_gbs, "decode_frac_hbm": s_gbs / world / peaks["hbm_gbs"],
+            "clocks": sc,
+            # time x clock: cycles per prefill launch at the median clock under load, against
+            # the timed region's (comparable when the work per cycle is unchanged)
+            "prefill_mcycles_per_launch": (pre_s / n_steps * mhz) if mhz else None,
+            "prefill_mcycles_per_launch_timed_region":
+                (pre_avg_s * clk.summary()["sm_mhz"]) if clk.summary().get("sm_mhz") else None,
+            "peak": f"bf16 sustained {tag} ({peaks['bf16_tflops_sustained']} TFLOP/s: cuBLAS "
+                    "bf16 GEMM looped for seconds under the power cap)"}
+
     cpu = None
     if rank == 0 and world == 1 and args.cpu_budget > 0:
         import oracle
@@ -612,6 +676,7 @@ def main():
             "softmax_exp": softmax_exp,
             "cpu_baseline": cpu,
             "e2e": e2e,
+            "sustained": sustained,
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clk.summary(),
         }

@@ -95,6 +95,8 @@ enum attn_status {
  *           kinds [1,Hq,N]; PAGED_DECODE and DECODE [B,Hq].
  * B         batch (dense), number of segments (document kinds) or sequences (decode kinds).
  * Hq, Hkv   query / key-value heads; Hq % Hkv == 0; query head h reads kv head h/(Hq/Hkv).
+ *           PAGED_DECODE and DECODE take at most 16 query heads per kv head (else
+ *           ATTN_ERR_UNSUPPORTED): the group's heads are the rows of one 16-row MMA tile.
  * N         keys per sequence (dense), packed tokens (document kinds), the longest context
  *           (PAGED_DECODE: block_table has ceil(N/page_size) columns), or the rows of each
  *           dense cache (DECODE).
@@ -222,8 +224,10 @@ int attn_gather_pages(const void *pool, void *dst, const int32_t *block_table, i
  * the library, held by every GPU that loads it until the process exits. Meant for callers that get no scratch buffer from
  * their host framework (a custom-op interface, another framework's memory pool) or must not
  * let cudaMalloc / cudaFree synchronise the device on a serving path. It allocates nothing.
- *  - Returns ATTN_ERR_UNSUPPORTED, with a message, when attn_workspace_bytes() of the request
- *    exceeds the array; nothing is launched then.
+ *  - Arguments are checked first as attn_fwd checks them (ATTN_ERR_INVALID or
+ *    ATTN_ERR_UNSUPPORTED with the reason). Then it returns ATTN_ERR_UNSUPPORTED, with a
+ *    message, when attn_workspace_bytes() of the request exceeds the array
+ *    (attn_noalloc_scratch_bytes()); nothing is launched then.
  *  - The first call on each device looks up the array's device address (cudaGetSymbolAddress)
  *    with that device current; make that first call before any stream capture.
  *  - Every call shares the one array per device and it keeps the last call's contents (the
@@ -234,6 +238,10 @@ int attn_paged_decode_noalloc(const void *q, const void *k, const void *v, void 
                               int B, int Hq, int Hkv, int N, int d, float scale,
                               const int32_t *cu_seqlens, const int32_t *block_table,
                               int page_size, int num_pages, void *stream);
+
+/* Size in bytes of attn_paged_decode_noalloc's fixed scratch array (16 MiB): a request is
+ * served iff attn_workspace_bytes() of it, with mask_kind PAGED_DECODE, is at most this. */
+size_t attn_noalloc_scratch_bytes(void);
 
 /* Synchronises `stream`, then returns and clears the device status word (ATTN_OK or one of
  * ATTN_ERR_TIMEOUT / ATTN_ERR_BOUNDS / ATTN_ERR_SEQLENS), or ATTN_ERR_CUDA if the stream
@@ -259,8 +267,16 @@ int attn_selftest_wait_timeout(unsigned long long timeout_ns, void *stream);
  * `stream`; the caller times it. Returns ATTN_OK, ATTN_ERR_INVALID or ATTN_ERR_CUDA. */
 int attn_bench_ex2(float *out, int blocks, int iters, void *stream);
 
-/* Frees the library's cached device state (status word) on the current device. */
+/* Forgets the library's cached device addresses on every device: the status word's and the
+ * allocation-free decode's scratch array's. Call it around cudaDeviceReset (or anything else
+ * that ends the context): the next call on a device looks both up again. Must not overlap
+ * other calls into the library. */
 void attn_release(void);
+
+/* Which device addresses the library has cached for `device`: bit 0 the status word's, bit 1
+ * the allocation-free decode's scratch array's (0 after attn_release). ATTN_ERR_INVALID for a
+ * device index outside [0, 64). Host-only; makes no CUDA call. */
+int attn_cached_device_state(int device);
 
 /* Library version, (major << 16) | minor. */
 int attn_version(void);

@@ -85,8 +85,10 @@ class _FakeDevicePtr:
 def test_decode_validation_before_cuda():
     t = _FakeDevicePtr()
     base = dict(q=t, k=t, v=t, o=t, lse=t, cu_seqlens=t, N=256)
-    # three query heads per kv head: no decode instantiation
-    assert _call(mask_kind=attn.ATTN_MASK_DECODE, Hq=3, Hkv=1, **base) == attn.ATTN_ERR_UNSUPPORTED
+    # more than 16 query heads per kv head: larger than one MMA tile of heads
+    assert _call(mask_kind=attn.ATTN_MASK_DECODE, Hq=17, Hkv=1, **base) == attn.ATTN_ERR_UNSUPPORTED
+    # three query heads per kv head are served (here the missing workspace is reported)
+    assert _call(mask_kind=attn.ATTN_MASK_DECODE, Hq=3, Hkv=1, **base) == attn.ATTN_ERR_WORKSPACE
     # workspace missing
     assert (_call(mask_kind=attn.ATTN_MASK_DECODE, Hq=4, Hkv=1, **base)
             == attn.ATTN_ERR_WORKSPACE)

@@ -100,9 +100,9 @@ def test_fp8_zero_key_tile():
     compare(w, run(w), strict=False)
 
 
-def test_fp8_headline_shape_sampled():
+def test_fp8_headline_shape():
     """Causal B2 Hq32 Hkv8 N8192 with Q / K quantized by the library (checked against the
-    oracle's quantizer byte for byte), attention on sampled rows against the oracle."""
+    oracle's quantizer byte for byte), attention on every output row against the oracle."""
     w = I.config("3c")
     B, Hq, Hkv, N = w.B, w.Hq, w.Hkv, w.N
     q8, qs = gpu_quantize(w.q.reshape(B * Hq, N, 128))
@@ -113,9 +113,4 @@ def test_fp8_headline_shape_sampled():
     assert np.array_equal(k8, rk8) and np.array_equal(ks, rks)
     w.q8, w.k8 = rq8.reshape(w.q.shape), rk8.reshape(w.k.shape)
     w.q_scales, w.k_scales = rqs, rks
-    dp = run(w)
-    rng = np.random.default_rng(10)
-    n = int(np.prod(w.lse_shape))
-    heads = np.arange(B * Hq) * N
-    rows = np.unique(np.concatenate([rng.integers(0, n, 2000), heads, heads + N - 1]))
-    compare(w, dp, rows=rows)
+    compare(w, run(w))

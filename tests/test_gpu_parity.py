@@ -71,16 +71,10 @@ def test_config2_causal():
     compare(w, run(w))
 
 
-def test_config3_sliding_gqa_sampled():
+def test_config3_sliding_gqa():
+    """Every one of the 524,288 output rows against the oracle."""
     w = I.config(3)
-    dp = run(w)
-    rng = np.random.default_rng(5)
-    n = int(np.prod(w.lse_shape))
-    # random rows plus every head's first and last row and the window edge rows
-    heads = np.arange(w.B * w.Hq) * w.N
-    rows = np.unique(np.concatenate([rng.integers(0, n, 3000), heads, heads + w.N - 1,
-                                     heads + 4095, heads + 4096, heads + 4223]))
-    compare(w, dp, rows=rows)
+    compare(w, run(w))
 
 
 def test_config4_document():
@@ -93,16 +87,11 @@ def test_config5_paged_decode():
     compare(w, run(w))
 
 
-def test_headline_causal_n8192_sampled():
+def test_headline_causal_n8192():
     """The causal B2 Hq32 Hkv8 N8192 d128 shape the throughput is quoted on, in the launch
-    configuration the benchmark times."""
+    configuration the benchmark times: every one of the 524,288 output rows."""
     w = I.config("3c")
-    dp = run(w)
-    rng = np.random.default_rng(6)
-    n = int(np.prod(w.lse_shape))
-    heads = np.arange(w.B * w.Hq) * w.N
-    rows = np.unique(np.concatenate([rng.integers(0, n, 3000), heads, heads + w.N - 1]))
-    compare(w, dp, rows=rows)
+    compare(w, run(w))
 
 
 # ------------------------------------------------------------------ ragged sweeps
@@ -185,7 +174,7 @@ def test_bidir_window_covering_equals_none_bit_exact():
 
 
 @pytest.mark.parametrize("d", [64, 128])
-@pytest.mark.parametrize("group", [1, 2, 4, 8])
+@pytest.mark.parametrize("group", [1, 2, 3, 4, 5, 6, 8, 12, 16])
 def test_paged_ragged(d, group):
     lens = [1, 63, 64, 65, 1000, 1025, 2048, 3000]
     w = I.paged_decode_workload(400 + group, len(lens), 0, 0, 2 * group, 2, d,
@@ -194,7 +183,7 @@ def test_paged_ragged(d, group):
 
 
 @pytest.mark.parametrize("d", [64, 128])
-@pytest.mark.parametrize("group", [1, 4, 16])
+@pytest.mark.parametrize("group", [1, 3, 4, 6, 11, 16])
 def test_dense_decode_ragged(d, group):
     """Decode on dense per-sequence caches; the cache is longer than every context and its
     tail holds poison, so reading past L_b would show."""
@@ -543,14 +532,14 @@ _FUZZ_KINDS = [I.MASK_NONE, I.MASK_CAUSAL, I.MASK_SLIDING, I.MASK_SLIDING_BIDIR,
 
 def _fuzz_workload(idx):
     """Case idx: its mask kind in turn, the rest drawn from a generator seeded by idx: head dim,
-    batch, GQA group (any divisor for prefill, 3 included; 1/2/4/8 for decode), lengths,
+    batch, GQA group (1-4 query heads per kv head for prefill, 1-16 for decode), lengths,
     windows and prefixes past the sequence, empty segments and chunks, page sizes."""
     rng = np.random.default_rng(5000 + idx)
     kind = _FUZZ_KINDS[idx % len(_FUZZ_KINDS)]
     d = int(rng.choice([64, 128]))
     Hkv = int(rng.integers(1, 4))
     decode = kind in (I.MASK_PAGED_DECODE, I.MASK_DECODE)
-    Hq = Hkv * int(rng.choice([1, 2, 4, 8]) if decode else rng.integers(1, 5))
+    Hq = Hkv * int(rng.integers(1, 17) if decode else rng.integers(1, 5))
     seed = 6000 + idx
     if kind in (I.MASK_DOCUMENT, I.MASK_DOCUMENT_BIDIR):
         lens = rng.integers(0, 400, int(rng.integers(1, 7)))

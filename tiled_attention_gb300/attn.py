@@ -60,6 +60,8 @@ _SIGS = {
     "attn_paged_decode_noalloc": (_i, [_p, _p, _p, _p, _p, _i, _i, _i, _i, _i, ctypes.c_float,
                                        _p, _p, _i, _i, _p]),
     "attn_bench_ex2": (_i, [_p, _i, _i, _p]),
+    "attn_noalloc_scratch_bytes": (ctypes.c_size_t, []),
+    "attn_cached_device_state": (_i, [_i]),
 }
 
 
@@ -183,6 +185,16 @@ def attn_get_status(stream=None) -> int:
 
 def attn_release() -> None:
     lib().attn_release()
+
+
+def attn_cached_device_state(device: int) -> int:
+    """Bit 0: the status word's address is cached for `device`; bit 1: the allocation-free
+    decode's scratch address is."""
+    return lib().attn_cached_device_state(device)
+
+
+def attn_noalloc_scratch_bytes() -> int:
+    return lib().attn_noalloc_scratch_bytes()
 
 
 def attn_version() -> int:

@@ -49,6 +49,14 @@ std::mutex g_mu;
 
 int g_num_sms[kMaxDevices];
 
+// Split-KV scratch of attn_paged_decode_noalloc, for callers that cannot allocate: one fixed
+// array per device, held from the library's load until the process exits. Its device address
+// is looked up once per device (cudaGetSymbolAddress) and cached here; attn_release forgets it
+// together with the status word's.
+constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;  // 16 MiB
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+void* g_noalloc_scratch_ptr[kMaxDevices];
+
 int sm_count(int* out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -165,6 +173,7 @@ bool window_ok(int m, int window) {
 
 constexpr unsigned long long kTimeoutNs = 2000000000ull;  // 2 s per pipeline wait
 constexpr int kDecodeStage = 64;       // tokens per decode ring stage
+constexpr int kMaxDecodeGroup = 16;    // query heads per kv head: the rows of one MMA tile
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct DecodeLayout {
@@ -433,8 +442,9 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
     } else if (static_cast<long long>(B) * Hkv >= (1ll << 31)) {
       return fail(ATTN_ERR_UNSUPPORTED, "B*Hkv too large");
     }
-    if (group != 1 && group != 2 && group != 4 && group != 8 && group != 16)
-      return fail(ATTN_ERR_UNSUPPORTED, "query heads per kv head %d (1, 2, 4, 8, 16)", group);
+    if (group > kMaxDecodeGroup)
+      return fail(ATTN_ERR_UNSUPPORTED, "query heads per kv head %d (at most %d)", group,
+                  kMaxDecodeGroup);
     L = decode_layout(B, Hq, Hkv, N, d);
     if (L.max_splits > 65535 || Hkv > 65535 || B > 65535)
       return fail(ATTN_ERR_UNSUPPORTED, "decode grid too large");
@@ -483,6 +493,7 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
     p.max_len = N;
     p.max_splits = L.max_splits;
     p.chunk_pages = L.chunk_pages;
+    p.group = group;
     p.scale_log2 = scale * kLog2e;
     p.status = status;
     p.timeout_ns = kTimeoutNs;
@@ -722,7 +733,16 @@ int attn_get_status(void* stream) {
 
 void attn_release(void) {
   std::lock_guard<std::mutex> lk(g_mu);
-  for (int i = 0; i < kMaxDevices; ++i) g_status_ptr[i] = nullptr;
+  for (int i = 0; i < kMaxDevices; ++i) {
+    g_status_ptr[i] = nullptr;
+    g_noalloc_scratch_ptr[i] = nullptr;
+  }
+}
+
+int attn_cached_device_state(int device) {
+  if (device < 0 || device >= kMaxDevices) return ATTN_ERR_INVALID;
+  std::lock_guard<std::mutex> lk(g_mu);
+  return (g_status_ptr[device] ? 1 : 0) | (g_noalloc_scratch_ptr[device] ? 2 : 0);
 }
 
 int attn_plan_kv_range(int mask_kind, int window, int r0, int bm, int row_end, int k_org,
@@ -816,14 +836,10 @@ int attn_plan_units(int mask_kind, int B, int Hq, int N, const int32_t* cu, int3
 // running inside another framework's device-memory pool or a custom-op interface that passes
 // no scratch buffer, and serving loops where the implicit device synchronisation of
 // cudaMalloc / cudaFree is not acceptable. attn_paged_decode_noalloc serves them: its
-// split-KV partials and tickets live in the fixed array below, which every GPU that loads
-// this library holds until the process exits.
+// split-KV partials and tickets live in g_noalloc_scratch (declared with the status word),
+// which every GPU that loads this library holds until the process exits.
 namespace ta {
 namespace {
-constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;  // 16 MiB
-static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
-void* g_noalloc_scratch_ptr[kMaxDevices];
-
 // Device address of the scratch array on the current device. In host code the array's name
 // is only a host-side stand-in, so the address comes from cudaGetSymbolAddress, once per
 // device, with that device current.
@@ -845,12 +861,25 @@ int noalloc_scratch(void** out) {
 }  // namespace
 }  // namespace ta
 
+extern "C" size_t attn_noalloc_scratch_bytes(void) { return kNoAllocScratchBytes; }
+
 extern "C" int attn_paged_decode_noalloc(const void* q, const void* k, const void* v, void* o,
                                          float* lse, int B, int Hq, int Hkv, int N, int d,
                                          float scale, const int32_t* cu_seqlens,
                                          const int32_t* block_table, int page_size,
                                          int num_pages, void* stream) {
   g_last_error.clear();
+  // The cheap argument checks come first, so that an invalid request reports its own reason
+  // rather than a scratch size computed from invalid arguments.
+  if (B < 0 || N < 0 || Hq <= 0 || Hkv <= 0)
+    return fail(ATTN_ERR_INVALID, "need B >= 0, N >= 0, Hq > 0, Hkv > 0");
+  if (Hq % Hkv != 0) return fail(ATTN_ERR_INVALID, "Hq (%d) %% Hkv (%d) != 0", Hq, Hkv);
+  if (d != 64 && d != 128) return fail(ATTN_ERR_UNSUPPORTED, "head dim %d (64 or 128)", d);
+  if (!page_size_ok(page_size))
+    return fail(ATTN_ERR_UNSUPPORTED, "page_size %d (16, 32, 64 or 128)", page_size);
+  if (Hq / Hkv > kMaxDecodeGroup)
+    return fail(ATTN_ERR_UNSUPPORTED, "query heads per kv head %d (at most %d)", Hq / Hkv,
+                kMaxDecodeGroup);
   const size_t need =
       attn_workspace_bytes(B, Hq, Hkv, N, d, ATTN_MASK_PAGED_DECODE, page_size);
   if (need > kNoAllocScratchBytes)

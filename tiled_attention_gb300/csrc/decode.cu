@@ -1,4 +1,5 @@
-// decode.cu — instantiations of the paged decode kernel (head dim 64 / 128, group 1 / 2 / 4 / 8).
+// decode.cu — instantiations of the paged decode kernel: head dim 64 / 128, and 1, 2, 4, 8 or
+// 16 tile rows of query heads (a group of G heads runs on the smallest that holds it).
 #include "launch.h"
 
 namespace ta {
@@ -19,14 +20,12 @@ cudaError_t launch_one(const CUtensorMap& k, const CUtensorMap& v, const DecodeP
 template <int D>
 cudaError_t launch_d(int group, const CUtensorMap& k, const CUtensorMap& v,
                      const DecodeParams& p, dim3 grid, cudaStream_t stream) {
-  switch (group) {
-    case 1: return launch_one<D, 1>(k, v, p, grid, stream);
-    case 2: return launch_one<D, 2>(k, v, p, grid, stream);
-    case 4: return launch_one<D, 4>(k, v, p, grid, stream);
-    case 8: return launch_one<D, 8>(k, v, p, grid, stream);
-    case 16: return launch_one<D, 16>(k, v, p, grid, stream);
-    default: return cudaErrorInvalidValue;
-  }
+  if (group < 1 || group > 16) return cudaErrorInvalidValue;
+  if (group == 1) return launch_one<D, 1>(k, v, p, grid, stream);
+  if (group == 2) return launch_one<D, 2>(k, v, p, grid, stream);
+  if (group <= 4) return launch_one<D, 4>(k, v, p, grid, stream);
+  if (group <= 8) return launch_one<D, 8>(k, v, p, grid, stream);
+  return launch_one<D, 16>(k, v, p, grid, stream);
 }
 }  // namespace
 

@@ -46,6 +46,7 @@ struct DecodeParams {
   float* part_ml;        // [B*Hkv, max_splits, G, 2]
   int* counters;         // [B*Hkv], zero before the launch
   int B, Hq, Hkv, max_pages, num_pages, max_splits, chunk_pages;
+  int group;             // query heads per kv head, Hq / Hkv (at most the kernel's tile rows)
   int page_shift;        // log2 of the tokens per pool page (paged: 4..7); a TMA box holds
                          // min(page_size, 64) rows
   int dense;             // 1: K/V are dense caches [B*Hkv, max_len, D], no block table
@@ -55,7 +56,7 @@ struct DecodeParams {
   unsigned long long timeout_ns;
 };
 
-template <int D, int G>
+template <int D, int G>  // G: tile rows holding query heads
 struct DecodeCfg {
   static constexpr int kPage = 64;  // tokens per ring stage
   static constexpr int kWarps = 4;  // consumer warp w owns tokens [16w, 16w + 16) of each page
@@ -117,12 +118,15 @@ __device__ __forceinline__ uint32_t page_chunk(int token, int d0) {
                                ((((d0 & 63) >> 3) ^ (token & 7)) << 4));
 }
 
-template <int D, int G>
+// GT: rows of the MMA tile that hold query heads (1, 2, 4, 8 or 16); the group's G = Hq / Hkv
+// heads (G <= GT) fill the first G, and the rest are computed on zero queries and dropped.
+template <int D, int GT>
 __global__ void __launch_bounds__(160, 2)
     decode_kernel(const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const DecodeParams p) {
-  using C = DecodeCfg<D, G>;
+  using C = DecodeCfg<D, GT>;
   constexpr int S = C::kStages;
+  const int G = p.group;  // query heads of the group, 1 <= G <= GT
   const int split = static_cast<int>(blockIdx.x);
   const int g = static_cast<int>(blockIdx.y);
   const int b = static_cast<int>(blockIdx.z);
@@ -495,7 +499,7 @@ __global__ void __launch_bounds__(160, 2)
   // output element then sums its splits from independent loads, in split order, so the
   // result is the same as a plain loop over the splits.
   const size_t base_bg = bg * p.max_splits * G;  // (b, g)'s first partial row
-  constexpr int kMergeCap = C::kRingBytes / (8 * G);  // splits whose (w, l) fit the ring
+  constexpr int kMergeCap = C::kRingBytes / (8 * GT);  // splits whose (w, l) fit the ring
   if (nsplit <= kMergeCap) {
     float* sw = reinterpret_cast<float*>(ring);  // [G][nsplit]: m, then the weight
     float* sl = sw + G * nsplit;                 // [G][nsplit]: l
