@@ -515,8 +515,9 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
   CUtensorMap tq, tk, tv, to;
   if ((rc = encode_3d(&tq, q, d, N, planes_q, 128))) return rc;
   if ((rc = encode_3d(&to, o, d, N, planes_q, 32))) return rc;
-  if ((rc = encode_3d(&tk, k, d, N, planes_kv, 128))) return rc;
-  if ((rc = encode_3d(&tv, v, d, N, planes_kv, 128))) return rc;
+  const uint32_t kv_rows = static_cast<uint32_t>(prefill_key_tile(d, mask_kind));
+  if ((rc = encode_3d(&tk, k, d, N, planes_kv, kv_rows))) return rc;
+  if ((rc = encode_3d(&tv, v, d, N, planes_kv, kv_rows))) return rc;
   PrefillParams p{};
   p.o = o;
   p.lse = lse;

@@ -65,10 +65,19 @@ struct PrefillParams {
   unsigned long long timeout_ns;
 };
 
-template <int D>
+// Key-tile width. 128 in general. At d = 64 (but for the paged kind, whose page boxes must
+// tile the key tile) 96: each query tile then holds two S buffers in TMEM (4 x 96 + 2 x 64 =
+// 512 columns), so S of the next key tile is computed while the softmax works on this one.
+__host__ __device__ constexpr int prefill_key_tile(int d, int mask) {
+  return d == 64 && mask != kMaskPagedPrefill ? 96 : 128;
+}
+
+template <int D, int BN_ = 128>
 struct PrefillCfg {
   static constexpr int BM = 128;
-  static constexpr int BN = 128;
+  static constexpr int BN = BN_;
+  // Two S buffers per query tile (see prefill_key_tile).
+  static constexpr bool kDoubleS = BN == 96;
   static constexpr int kThreads = 384;
   static constexpr int kChunkBytes = BM * 128;        // one 64-column, 128-row swizzle panel
   static constexpr int kPanels = D / 64;
@@ -81,7 +90,8 @@ struct PrefillCfg {
   static constexpr int kQBufs = 3;
   static constexpr int kStagesFit =
       (kSmemLimit - 1024 - kCtrlBytes - kQBufs * kQBytes) / kKVBytes;
-  static constexpr int kStages = kStagesFit > 8 ? 8 : kStagesFit;
+  static constexpr int kMaxStages = kDoubleS ? 12 : 8;
+  static constexpr int kStages = kStagesFit > kMaxStages ? kMaxStages : kStagesFit;
   static constexpr int kSmemBytes = 1024 + kQBufs * kQBytes + kStages * kKVBytes + kCtrlBytes;
   static constexpr int kTmemCols = 512;
   // Launch: 384 threads x 168 registers = 64512. Warpgroup 0 (producer, MMA, two idle warps)
@@ -92,17 +102,24 @@ struct PrefillCfg {
   static constexpr uint32_t kIdescO = idesc_bf16(BM, D, false, true);    // V is MN-major
 };
 
+template <int ST>
 struct PrefillCtrl {
   uint64_t q_full[3];
   uint64_t q_empty[3];  // the epilogue that staged O in the buffer has finished with it
-  uint64_t kv_full[8];
-  uint64_t kv_empty[8];
+  uint64_t kv_full[ST];
+  uint64_t kv_empty[ST];
   uint64_t s_ready[2];
   uint64_t p_ready[2];
   uint64_t o_done[2];
-  uint64_t drain;
+  uint64_t drain[2];  // [1]: the second issuing warp (two S buffers)
   uint32_t tmem_base;
   int abort_flag;
+  // Two S buffers per query tile: S ready, P ready and P.V done per (query tile, buffer).
+  // One barrier per buffer keeps every parity wait unambiguous: a buffer's next phase needs
+  // the consumer of its current one to have moved on.
+  uint64_t s_ready2[2][2];
+  uint64_t p_ready2[2][2];
+  uint64_t pv_done[2][2];
 };
 
 struct Unit {
@@ -321,8 +338,14 @@ __global__ void __launch_bounds__(384, 1)
                    const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v,
                    const __grid_constant__ CUtensorMap tm_o, const PrefillParams p) {
-  using C = PrefillCfg<D>;
+  using C = PrefillCfg<D, prefill_key_tile(D, MASK)>;
   constexpr int BM = C::BM, BN = C::BN, STAGES = C::kStages, QB = C::kQBufs;
+  constexpr bool kDB = C::kDoubleS;
+  static_assert(!kDB || (D == 64 && !FP8 && MASK != kMaskPagedPrefill), "double S: d = 64");
+  // TMEM columns: S (or P) of query tile i, buffer b; the O accumulators after them.
+  constexpr int kSBufs = kDB ? 2 : 1;
+  constexpr int kOCol = 2 * kSBufs * BN;
+  static_assert(kOCol + 2 * D <= C::kTmemCols, "TMEM columns");
   // Visit tile 1's extra key tiles first (see geometry below): at d = 64, for the kinds whose
   // two query tiles can end on different key tiles. Measured on GB300: 5.5 % faster for the
   // causal document workload at d = 64, where the softmax chain dominates; slower at d = 128,
@@ -350,8 +373,9 @@ __global__ void __launch_bounds__(384, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* q_s = smem;                                  // [QB][kQBytes]
   uint8_t* kv_s = smem + QB * C::kQBytes;               // [STAGES][kKVBytes]
-  PrefillCtrl* ctl = reinterpret_cast<PrefillCtrl*>(kv_s + STAGES * C::kKVBytes);
-  static_assert(sizeof(PrefillCtrl) <= C::kCtrlBytes, "control block");
+  using Ctrl = PrefillCtrl<C::kMaxStages>;
+  Ctrl* ctl = reinterpret_cast<Ctrl*>(kv_s + STAGES * C::kKVBytes);
+  static_assert(sizeof(Ctrl) <= C::kCtrlBytes, "control block");
 
   const int warp = static_cast<int>(threadIdx.x >> 5);
   const int lane = static_cast<int>(lane_id());
@@ -370,9 +394,18 @@ __global__ void __launch_bounds__(384, 1)
       }
       for (int s = 0; s < STAGES; ++s) {
         mbar_init(&ctl->kv_full[s], 1);
-        mbar_init(&ctl->kv_empty[s], 1);
+        mbar_init(&ctl->kv_empty[s], kDB ? 2 : 1);  // one release per issuing warp
       }
-      mbar_init(&ctl->drain, 1);
+      if constexpr (kDB) {
+        for (int i = 0; i < 2; ++i)
+          for (int bb = 0; bb < 2; ++bb) {
+            mbar_init(&ctl->s_ready2[i][bb], 1);
+            mbar_init(&ctl->p_ready2[i][bb], 128);
+            mbar_init(&ctl->pv_done[i][bb], 1);
+          }
+      }
+      mbar_init(&ctl->drain[0], 1);
+      mbar_init(&ctl->drain[1], 1);
       fence_mbar_init();
       prefetch_tensormap(&tm_q);
       prefetch_tensormap(&tm_k);
@@ -532,12 +565,119 @@ __global__ void __launch_bounds__(384, 1)
         for (int x = imax(0, qn - QB); x < qn; ++x)
           mbar_wait(&ctl->q_full[x % QB], (x / QB) & 1, wc_drain);
       }
-    } else if (warp == 1) {
+    } else if (warp == 1 || (kDB && warp == 2)) {
       // -------------------------------------------------------------- MMA issuer
       // The whole warp runs this loop, so descriptors and loop state are warp-uniform; one
       // elected lane issues each tcgen05 instruction (see mma_ss). Waits are agreed on by the
       // whole warp so it never diverges.
       constexpr unsigned kFull = 0xffffffffu;
+      if constexpr (kDB) {
+        // Two S buffers per query tile and one issuing warp per query tile: warp 1 issues
+        // tile 0's MMAs, warp 2 tile 1's (one warp for both spent most of each key tile on
+        // barrier checks and bookkeeping, on a sub-partition shared with two softmax warps,
+        // and fell behind the softmax). Position x of a unit is its x-th key tile in visiting
+        // order (kv_at); its K is ring entry e + 2x, its V e + 2x + 1. The S of positions 0
+        // and 1 go first; step x issues P.V of position x and then the S of position x + 2
+        // into the buffer that P.V has just read (MMAs of one thread run in order), so the
+        // tile's next S is computed while its softmax works on the current one. Every ring
+        // entry takes one release from each issuer (kv_empty counts two), and each issuer
+        // waits for an entry to land before releasing it, used or not, so neither can release
+        // a slot ahead of its refill.
+        const int i = warp - 1;  // this warp's query tile
+        int e = 0;               // ring entry of the unit's first K
+        int qc = 0;              // Q loads of both tiles before this unit
+        int sn = 0;              // S tiles issued so far (buffer sn & 1)
+        int pn = 0;              // P tiles consumed so far (buffer pn & 1)
+        bool ok = true;
+        for (int k = 0; ok; ++k) {
+          const int u = unit_of(k);
+          if (u >= p.num_units) break;
+          const Unit un = decode_unit<MASK>(u, p, cur);  // warp-collective
+          if (!un.valid) break;
+          KvRange rng[2];
+          int lo, hi;
+          geometry(un, rng, lo, hi);
+          const int e1 = kRot ? extra_of(rng) : 0;
+          const int npos = hi - lo;
+          const int n0 = rng[0].hi > rng[0].lo ? 1 : 0, n1 = rng[1].hi > rng[1].lo ? 1 : 0;
+          const int qn = i == 0 ? qc : qc + n0;  // this tile's Q load
+          const uint64_t q_desc = sw128_desc(smem_u32(q_s + (qn % QB) * C::kQBytes), 16, 1024);
+          const int rlo = i ? rng[1].lo : rng[0].lo, rhi = i ? rng[1].hi : rng[0].hi;
+          const int tlen = rhi - rlo;
+          // Index of key tile j in this tile's own visiting order (see tile_index).
+          auto my_index = [&](int j) {
+            return (kRot && i == 1) ? (j >= hi - e1 ? j - (hi - e1) : j - rlo + e1) : j - rlo;
+          };
+          auto key_at = [&](int x) { return kRot ? kv_at(x, lo, hi, e1) : lo + x; };
+          auto wait_entry = [&](int en) {
+            return __all_sync(kFull,
+                              mbar_wait(&ctl->kv_full[en % STAGES], (en / STAGES) & 1, wc));
+          };
+          // S of position x (if this tile sees that key tile), then release K of x.
+          auto do_k = [&](int x) -> bool {
+            const int en = e + 2 * x;
+            if (!wait_entry(en)) return false;
+            tc_fence_after();
+            const int j = key_at(x);
+            if (j >= rlo && j < rhi) {
+              if (my_index(j) == 0) {  // the tile's first S: its Q
+                if (!__all_sync(kFull, mbar_wait(&ctl->q_full[qn % QB], (qn / QB) & 1, wc)))
+                  return false;
+                tc_fence_after();
+              }
+              const int buf = sn & 1;
+              const uint32_t d_s = tmem + (i * 2 + buf) * BN;
+              const uint64_t k_desc =
+                  sw128_desc(smem_u32(kv_s + (en % STAGES) * C::kKVBytes), 16, 1024);
+#pragma unroll
+              for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t off16 = ((kk >> 2) * C::kChunkBytes + (kk & 3) * 32) >> 4;
+                mma_ss(d_s, q_desc + off16, k_desc + off16, C::kIdescS, kk > 0 ? 1u : 0u);
+              }
+              mma_commit(&ctl->s_ready2[i][buf]);
+              ++sn;
+            }
+            mma_commit(&ctl->kv_empty[en % STAGES]);
+            return true;
+          };
+          // P.V of position x into O (the tile's first one overwrites it), then release V.
+          auto do_v = [&](int x) -> bool {
+            const int en = e + 2 * x + 1;
+            if (!wait_entry(en)) return false;
+            tc_fence_after();
+            const int j = key_at(x);
+            if (j >= rlo && j < rhi) {
+              const int buf = pn & 1;
+              if (!__all_sync(kFull, mbar_wait(&ctl->p_ready2[i][buf], (pn >> 1) & 1, wc)))
+                return false;
+              tc_fence_after();
+              const int t = my_index(j);
+              const uint32_t d_o = tmem + kOCol + i * D;
+              const uint32_t a_p = tmem + (i * 2 + buf) * BN;
+              const uint64_t v_desc =
+                  sw128_desc(smem_u32(kv_s + (en % STAGES) * C::kKVBytes), C::kChunkBytes, 1024);
+#pragma unroll
+              for (int kk = 0; kk < BN / 16; ++kk)
+                mma_ts(d_o, a_p + kk * 8, v_desc + kk * (2048 >> 4), C::kIdescO,
+                       kk > 0 ? 1u : (t > 0 ? 1u : 0u));
+              mma_commit(&ctl->pv_done[i][buf]);
+              if (t + 1 == tlen) mma_commit(&ctl->o_done[i]);
+              ++pn;
+            }
+            mma_commit(&ctl->kv_empty[en % STAGES]);
+            return true;
+          };
+          bool okk = true;
+          for (int x = 0; x < 2 && x < npos && okk; ++x) okk = do_k(x);
+          for (int x = 0; x < npos && okk; ++x) {
+            okk = do_v(x);
+            if (okk && x + 2 < npos) okk = do_k(x + 2);
+          }
+          ok = okk;
+          e += 2 * npos;
+          qc += n0 + n1;
+        }
+      } else {
       int e = 0;              // ring entry of the next K
       int qc = 0;             // Q loads consumed before this unit
       int pb0 = 0, pb1 = 0;   // P tiles consumed before this unit, per query tile
@@ -633,9 +773,10 @@ __global__ void __launch_bounds__(384, 1)
         pb0 += imax(rng[0].hi - rng[0].lo, 0);
         pb1 += imax(rng[1].hi - rng[1].lo, 0);
       }
+      }
       // Every MMA this warp issued has completed before TMEM can be released.
-      mma_commit(&ctl->drain);
-      mbar_wait(&ctl->drain, 0, wc_drain);
+      mma_commit(&ctl->drain[warp - 1]);
+      mbar_wait(&ctl->drain[warp - 1], 0, wc_drain);
     }
   } else {
     regs_increase<C::kRegsSoftmax>();
@@ -645,7 +786,7 @@ __global__ void __launch_bounds__(384, 1)
     const int r = quarter * 32 + lane;      // row inside the tile
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const uint32_t s_col = lane_base + i * 128;
-    const uint32_t o_col = lane_base + 256 + i * D;
+    const uint32_t o_col = lane_base + kOCol + i * D;
     const float c0 = p.scale_log2;
     int sc = 0, oc = 0;  // S tiles and finished units of this query tile consumed
     int pending_q = -1;  // tile 1: Q buffer whose O store may still be reading it
@@ -695,6 +836,108 @@ __global__ void __launch_bounds__(384, 1)
             FP8 ? fmaxf(cq * __ldg(p.k_scales + static_cast<size_t>(un.kvh) * p.nbk + j),
                         FLT_MIN)
                 : c0;
+        if constexpr (kDB) {
+          // Key tiles of 96: three 32-column chunks, S in buffer sc & 1 of this tile.
+          const int sbuf = sc & 1;
+          ok = __all_sync(0xffffffffu, mbar_wait(&ctl->s_ready2[i][sbuf], (sc >> 1) & 1, wc));
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t sb_col = lane_base + (i * 2 + sbuf) * BN;
+          uint32_t s0[32], s1[32], s2[32];
+          tmem_ld_x32(sb_col + 0, s0);
+          tmem_ld_x32(sb_col + 32, s1);
+          tmem_ld_x32(sb_col + 64, s2);
+          tmem_wait_ld_x32(s0);
+          tmem_wait_ld_x32(s1);
+          tmem_wait_ld_x32(s2);
+          float* f0 = reinterpret_cast<float*>(s0);
+          float* f1 = reinterpret_cast<float*>(s1);
+          float* f2 = reinterpret_cast<float*>(s2);
+          const int kind = tile_kind(MASK, p.window, q_row0 + i * BM, BM, row_end, k_org,
+                                     k_end, BN, j);
+          if (kind == kTileBoundary) {
+            const int key0 = k_org + j * BN;
+            const int lo_k = vis_lo(MASK, p.window, k_org, row) - key0;
+            const int hi_k = vis_hi(MASK, p.window, k_end, row) - key0;
+            if constexpr (kBitMask) {
+              const uint32_t b0 = vis_bits32(lo_k, hi_k), b1 = vis_bits32(lo_k - 32, hi_k - 32);
+              const uint32_t b2 = vis_bits32(lo_k - 64, hi_k - 64);
+              if (!__all_sync(0xffffffffu, b0 == 0xffffffffu)) {
+#pragma unroll
+                for (int t = 0; t < 32; ++t)
+                  if (!(b0 & (1u << t))) f0[t] = -INFINITY;
+              }
+              if (!__all_sync(0xffffffffu, b1 == 0xffffffffu)) {
+#pragma unroll
+                for (int t = 0; t < 32; ++t)
+                  if (!(b1 & (1u << t))) f1[t] = -INFINITY;
+              }
+              if (!__all_sync(0xffffffffu, b2 == 0xffffffffu)) {
+#pragma unroll
+                for (int t = 0; t < 32; ++t)
+                  if (!(b2 & (1u << t))) f2[t] = -INFINITY;
+              }
+            } else {
+#pragma unroll
+              for (int t = 0; t < 32; ++t) {
+                if (t < lo_k || t > hi_k) f0[t] = -INFINITY;
+                if (t + 32 < lo_k || t + 32 > hi_k) f1[t] = -INFINITY;
+                if (t + 64 < lo_k || t + 64 > hi_k) f2[t] = -INFINITY;
+              }
+            }
+          }
+          // Row max: three independent chains of 3-input max over the 96 scores.
+          float mx0 = fmax3(f0[0], f0[1], f0[2]), mx1 = fmax3(f1[0], f1[1], f1[2]);
+          float mx2 = fmax3(f2[0], f2[1], f2[2]);
+#pragma unroll
+          for (int t = 3; t < 31; t += 2) {
+            mx0 = fmax3(mx0, f0[t], f0[t + 1]);
+            mx1 = fmax3(mx1, f1[t], f1[t + 1]);
+            mx2 = fmax3(mx2, f2[t], f2[t + 1]);
+          }
+          mx0 = fmax3(mx0, f0[31], f1[31]);
+          const float m_tile = fmax3(mx0, mx1, fmaxf(mx2, f2[31])) * c;
+          float alpha = 1.f;
+          if (m_tile > m_run + 8.f) {
+            alpha = fast_exp2(m_run - m_tile);  // 0 when m_run is -inf
+            m_run = m_tile;
+          }
+          if (j0 > my.lo && __any_sync(0xffffffffu, alpha < 1.f)) {
+            // O holds this tile's previous P.V only once that MMA has finished: here S of
+            // this key tile was issued before it, so wait for it explicitly.
+            const int pv = sc - 1;
+            ok = __all_sync(0xffffffffu,
+                            mbar_wait(&ctl->pv_done[i][pv & 1], (pv >> 1) & 1, wc));
+            if (!ok) break;
+            tc_fence_after();
+#pragma unroll
+            for (int cc = 0; cc < D / 16; ++cc) {
+              uint32_t ov[16];
+              tmem_ld_x16(o_col + cc * 16, ov);
+              tmem_wait_ld_x16(ov);
+#pragma unroll
+              for (int t = 0; t < 16; ++t)
+                ov[t] = __float_as_uint(__uint_as_float(ov[t]) * alpha);
+              tmem_st_x16(o_col + cc * 16, ov);
+            }
+          }
+          const float msub = (m_run == -INFINITY) ? 0.f : m_run;
+          const float2 cc2 = make_float2(c, c);
+          const float2 mm = make_float2(-msub, -msub);
+          float2 sa = make_float2(0.f, 0.f), sb = make_float2(0.f, 0.f);
+          uint32_t pk[16];
+          exp2_pack_32(f0, cc2, mm, sa, sb, pk);
+          tmem_st_x16(sb_col + 0, pk);
+          exp2_pack_32(f1, cc2, mm, sa, sb, pk);
+          tmem_st_x16(sb_col + 16, pk);
+          exp2_pack_32(f2, cc2, mm, sa, sb, pk);
+          tmem_st_x16(sb_col + 32, pk);
+          l_run = l_run * alpha + ((sa.x + sa.y) + (sb.x + sb.y));
+          tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(&ctl->p_ready2[i][sbuf]);
+          ++sc;
+        } else {
         ok = __all_sync(0xffffffffu, mbar_wait(&ctl->s_ready[i], (sc++) & 1, wc));
         if (!ok) break;
         tc_fence_after();
@@ -804,6 +1047,7 @@ __global__ void __launch_bounds__(384, 1)
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(&ctl->p_ready[i]);
+        }
         release_pending();
       }
       if (!ok) break;

@@ -10,10 +10,10 @@ cudaError_t launch_one(const CUtensorMap& q, const CUtensorMap& k, const CUtenso
                        cudaStream_t stream) {
   static unsigned long long done = 0;
   auto kern = prefill_kernel<64, MASK>;
-  constexpr int smem = PrefillCfg<64>::kSmemBytes;
+  constexpr int smem = PrefillCfg<64, prefill_key_tile(64, MASK)>::kSmemBytes;
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), smem, &done);
   if (e != cudaSuccess) return e;
-  kern<<<grid, PrefillCfg<64>::kThreads, smem, stream>>>(q, k, v, o, p);
+  kern<<<grid, PrefillCfg<64, prefill_key_tile(64, MASK)>::kThreads, smem, stream>>>(q, k, v, o, p);
   return cudaGetLastError();
 }
 }  // namespace
