@@ -53,6 +53,32 @@ def test_quantizer_bit_exact(N, d):
     assert np.array_equal(codes, rc)
 
 
+def test_quantizer_bit_exact_stress():
+    """Many blocks over a wide range of magnitudes, blocks whose scale is a power of two with
+    values on E4M3 rounding midpoints, negative zeros, and blocks whose scale is an fp32
+    subnormal: codes and scales equal the oracle's quantizer byte for byte."""
+    rng = np.random.default_rng(2024)
+    planes, N, d = 64, 1024, 128
+    x = rng.standard_normal((planes, N, d)).astype(np.float32)
+    x *= (10.0 ** rng.uniform(-20, 20, (planes, 1, 1))).astype(np.float32)
+    # scale 2^-3 exactly (amax 448 * 2^-3), values on midpoints between E4M3 codes
+    mids = np.array([0.5 * (a + b) for a, b in zip(fp8.e4m3_values()[:-1], fp8.e4m3_values()[1:])
+                     if 0 < a and b <= 448], dtype=np.float32)
+    blk = rng.choice(mids, (128, d)).astype(np.float32) * np.float32(0.125)
+    blk *= np.where(rng.random((128, d)) < 0.5, -1, 1).astype(np.float32)
+    blk[0, 0] = 448 * 0.125
+    x[0, :128] = blk
+    x[1, 5, :] = -0.0                                   # negative zeros in a normal block
+    x[2, :128] = rng.standard_normal((128, d)).astype(np.float32) * np.float32(1e-38)
+    x[3, 128:256] = np.float32(-0.0)                    # a block of negative zeros only
+    bits = I.f32_to_bf16_bits(x)
+    codes, scales = gpu_quantize(bits)
+    rc, rs = fp8.quantize_blocks(bits)
+    assert np.array_equal(scales, rs)
+    bad = np.argwhere(codes != rc)
+    assert bad.size == 0, f"{len(bad)} codes differ, first at {bad[0]}"
+
+
 def fp8_workload(seed, B, Hq, Hkv, N, mask, window=0):
     w = I.dense_workload(seed, B, Hq, Hkv, N, 128, mask, window=window)
     w.q8, w.q_scales = fp8.quantize_blocks(w.q.reshape(B * Hq, N, 128))

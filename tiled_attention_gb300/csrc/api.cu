@@ -265,6 +265,15 @@ __global__ void gather_pages_kernel(const uint4* __restrict__ pool, uint4* __res
 // E4M3(x / scale) rounded to nearest even with saturation, the division again IEEE fp32. An
 // all-zero block gets scale 0 and zero codes. This is the block quantization of the
 // FlashAttention-3 page ("FP8 Block Quantization"), one scale per 128-row tile.
+//
+// Every element of a block is divided by the same scale s, so the correctly rounded quotient
+// x / s comes from Markstein's correction step (P. Markstein, "Computation of elementary
+// functions on the IBM RISC System/6000 processor", IBM J. Res. Dev. 34(1), 1990; also
+// Muller et al., "Handbook of Floating-Point Arithmetic", the division chapter): with
+// y = RN(1/s) and q = RN(x * y) (within one ulp of x / s), the remainder r = x - q * s is exact
+// in one FMA, and RN(q + r * y) is RN(x / s). That is one multiply and two FMAs per element
+// instead of a full division. A zero quotient keeps the sign of q (x = -0 gives -0), and a
+// block whose reciprocal is not finite (s below 2^-126) divides element by element.
 constexpr int kFp8Block = 128;
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
@@ -277,54 +286,115 @@ __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
   return r;
 }
 
-__global__ void __launch_bounds__(256)
-    quantize_fp8_kernel(const uint4* __restrict__ x, uint2* __restrict__ x8,
-                        float* __restrict__ scales, int N, int d, int nb) {
-  const int t = static_cast<int>(blockIdx.x);
-  const int pl = static_cast<int>(blockIdx.y);
-  const int r0 = t * kFp8Block;
-  const int rows = imin(kFp8Block, N - r0);
-  const size_t base = (static_cast<size_t>(pl) * N + r0) * d / 8;  // 8-element vectors
-  const int nvec = rows * d / 8;  // at most 128 * 128 / 8 = 2048: 8 per thread
-  __shared__ float red[8];
+// Persistent: CTA c takes blocks c, c + G, c + 2G, ... of the (plane, 128-row block) list. A
+// block is contiguous in memory (rows x d bf16), so one thread brings it into shared memory
+// with one bulk copy, and the next block's copy is in flight while this one is converted (two
+// buffers): loads overlap the reduction and the conversion instead of following them.
+constexpr int kQuantThreads = 256;
+constexpr int kQuantBufBytes = kFp8Block * 128 * 2;  // one block: 128 rows x d <= 128 bf16
+constexpr int kQuantSmemBytes = 2 * kQuantBufBytes + 64;
+
+__global__ void __launch_bounds__(kQuantThreads)
+    quantize_fp8_kernel(const uint8_t* __restrict__ x, uint2* __restrict__ x8,
+                        float* __restrict__ scales, int N, int d, int nb, int nblocks,
+                        int* status, unsigned long long timeout_ns) {
+  extern __shared__ __align__(128) uint8_t qsm[];
+  uint64_t* bar = reinterpret_cast<uint64_t*>(qsm + 2 * kQuantBufBytes);
+  __shared__ float red[kQuantThreads / 32];
   __shared__ float s_scale;
-  // The block is read from global memory once and kept in registers for both passes.
-  constexpr int kPer = kFp8Block * 128 / 8 / 256;
-  uint4 v[kPer];
-  float amax = 0.f;
-#pragma unroll
-  for (int k = 0; k < kPer; ++k) {
-    const int idx = static_cast<int>(threadIdx.x) + k * 256;
-    v[k] = idx < nvec ? x[base + idx] : make_uint4(0u, 0u, 0u, 0u);
-    const uint32_t w[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
-#pragma unroll
-    for (int e = 0; e < 4; ++e)
-      amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(w[e])), fabsf(bf16_hi(w[e]))));
-  }
-  for (int off = 16; off; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    float m = red[0];
-    for (int w = 1; w < static_cast<int>(blockDim.x >> 5); ++w) m = fmaxf(m, red[w]);
-    const float sc = __fdiv_rn(m, 448.f);
-    s_scale = sc;
-    scales[static_cast<size_t>(pl) * nb + t] = sc;
+  __shared__ int s_abort;
+  const int tid = static_cast<int>(threadIdx.x);
+  if (tid == 0) {
+    mbar_init(&bar[0], 1);
+    mbar_init(&bar[1], 1);
+    s_abort = 0;
+    fence_mbar_init();
   }
   __syncthreads();
-  const float sc = s_scale;
-#pragma unroll
-  for (int k = 0; k < kPer; ++k) {
-    const int idx = static_cast<int>(threadIdx.x) + k * 256;
-    if (idx >= nvec) break;
-    const uint32_t w[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
-    uint32_t c[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e)
-      c[e] = sc == 0.f ? 0u
-                       : e4m3x2(__fdiv_rn(bf16_lo(w[e]), sc), __fdiv_rn(bf16_hi(w[e]), sc));
-    x8[base + idx] = make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
+  const WaitCtl wc{timeout_ns, status, &s_abort};
+  const WaitCtl wc_drain{timeout_ns, status, nullptr};
+  auto issue = [&](int t, int slot) {  // one thread
+    const int pl = t / nb, r0 = (t % nb) * kFp8Block;
+    const uint32_t bytes = static_cast<uint32_t>(imin(kFp8Block, N - r0) * d * 2);
+    mbar_arrive_expect_tx(&bar[slot], bytes);
+    bulk_load(qsm + slot * kQuantBufBytes, x + (static_cast<size_t>(pl) * N + r0) * d * 2, bytes,
+              &bar[slot]);
+  };
+  const int G = static_cast<int>(gridDim.x);
+  int t = static_cast<int>(blockIdx.x);
+  int issued = 0;  // copies issued by thread 0
+  if (tid == 0 && t < nblocks) {
+    issue(t, 0);
+    issued = 1;
   }
+  int k = 0;
+  for (; t < nblocks; t += G, ++k) {
+    const int slot = k & 1;
+    // The other buffer was last read in the previous iteration, before its closing barrier.
+    if (tid == 0 && t + G < nblocks) {
+      issue(t + G, slot ^ 1);
+      ++issued;
+    }
+    const bool ok = mbar_wait(&bar[slot], (k >> 1) & 1, wc);
+    if (!__syncthreads_and(ok)) break;
+    const int pl = t / nb, bt = t % nb, r0 = bt * kFp8Block;
+    const int nvec = imin(kFp8Block, N - r0) * d / 8;  // 8-element vectors of the block
+    const uint4* v = reinterpret_cast<const uint4*>(qsm + slot * kQuantBufBytes);
+    float amax = 0.f;
+    for (int i = tid; i < nvec; i += kQuantThreads) {
+      const uint4 q = v[i];
+      const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(w[e])), fabsf(bf16_hi(w[e]))));
+    }
+    for (int off = 16; off; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    if ((tid & 31) == 0) red[tid >> 5] = amax;
+    __syncthreads();
+    if (tid == 0) {
+      float m = red[0];
+      for (int w = 1; w < kQuantThreads / 32; ++w) m = fmaxf(m, red[w]);
+      const float sc = __fdiv_rn(m, 448.f);
+      s_scale = sc;
+      scales[static_cast<size_t>(pl) * nb + bt] = sc;
+    }
+    __syncthreads();
+    const float sc = s_scale;
+    uint2* out = x8 + (static_cast<size_t>(pl) * N + r0) * d / 8;
+    const float rc = sc == 0.f ? 0.f : __frcp_rn(sc);
+    if (sc == 0.f) {
+      for (int i = tid; i < nvec; i += kQuantThreads) out[i] = make_uint2(0u, 0u);
+    } else if (isfinite(rc)) {
+      // Markstein's correction (see above); a zero quotient keeps the sign of the product.
+      auto quot = [&](float xv) {
+        const float q = xv * rc;
+        const float q1 = __fmaf_rn(__fmaf_rn(-q, sc, xv), rc, q);
+        return q1 == 0.f ? q : q1;
+      };
+      for (int i = tid; i < nvec; i += kQuantThreads) {
+        const uint4 q = v[i];
+        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+        uint32_t c[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) c[e] = e4m3x2(quot(bf16_lo(w[e])), quot(bf16_hi(w[e])));
+        out[i] = make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
+      }
+    } else {
+      for (int i = tid; i < nvec; i += kQuantThreads) {
+        const uint4 q = v[i];
+        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+        uint32_t c[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          c[e] = e4m3x2(__fdiv_rn(bf16_lo(w[e]), sc), __fdiv_rn(bf16_hi(w[e]), sc));
+        out[i] = make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
+      }
+    }
+    __syncthreads();  // this buffer, red and s_scale are free again
+  }
+  // After a timeout, let copies still in flight land before the CTA exits.
+  if (tid == 0)
+    for (int j = k; j < issued; ++j) mbar_wait(&bar[j & 1], (j >> 1) & 1, wc_drain);
 }
 
 // Self-test of the bounded pipeline wait: one thread waits on an mbarrier that nothing
@@ -620,9 +690,23 @@ int attn_quantize_fp8(const void* x, void* x8, float* scales, int planes, int N,
     return fail(ATTN_ERR_INVALID, "x and x8 must be 16-byte aligned, scales 4-byte aligned");
   if (planes > 65535) return fail(ATTN_ERR_UNSUPPORTED, "planes %d > 65535", planes);
   const int nb = (N + kFp8Block - 1) / kFp8Block;
-  quantize_fp8_kernel<<<dim3(nb, planes), 256, 0, static_cast<cudaStream_t>(stream)>>>(
-      static_cast<const uint4*>(x), static_cast<uint2*>(x8), scales, N, d, nb);
-  cudaError_t e = cudaGetLastError();
+  if (static_cast<long long>(nb) * planes >= (1ll << 31) - (1ll << 20))
+    return fail(ATTN_ERR_UNSUPPORTED, "too many 128-row blocks");
+  const int nblocks = nb * planes;
+  int* status = nullptr;
+  int rc = status_ptr(&status);
+  if (rc) return rc;
+  int sms = 0;
+  if ((rc = sm_count(&sms))) return rc;
+  static unsigned long long done = 0;
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(quantize_fp8_kernel),
+                                   kQuantSmemBytes, &done);
+  if (e != cudaSuccess) return cuda_fail(e, "quantize smem attribute");
+  const int grid = nblocks < 3 * sms ? nblocks : 3 * sms;  // three CTAs per SM
+  quantize_fp8_kernel<<<grid, kQuantThreads, kQuantSmemBytes, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<const uint8_t*>(x), static_cast<uint2*>(x8), scales, N, d, nb, nblocks, status,
+      kTimeoutNs);
+  e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "quantize launch");
   return ATTN_OK;
 }
