@@ -104,6 +104,28 @@ def test_dense_ragged(d, N, mask):
     compare(w, run(w), strict=False)
 
 
+@pytest.mark.parametrize("mask,window", [(I.MASK_NONE, 0), (I.MASK_CAUSAL, 0),
+                                         (I.MASK_SLIDING, 95), (I.MASK_SLIDING, 97),
+                                         (I.MASK_SLIDING, 192), (I.MASK_SLIDING_BIDIR, 96),
+                                         (I.MASK_PREFIX_LM, 97)])
+@pytest.mark.parametrize("N", [95, 96, 97, 191, 193, 287, 289, 385, 577])
+def test_d64_key_tile_edges(mask, window, N):
+    """d = 64 runs on 96-key tiles against 128-row query tiles: lengths, windows and prefixes
+    on either side of multiples of 96 put the diagonal and the window edges at every offset
+    inside a key tile, and key tiles across the query tiles' boundaries."""
+    w = I.dense_workload(700 + N + window, 2, 4, 2, N, 64, mask, window=window)
+    compare(w, run(w), strict=False)
+
+
+@pytest.mark.parametrize("lens", [[96, 95, 97], [192, 1, 288, 96], [383, 385, 96, 97, 191]])
+@pytest.mark.parametrize("mask", [I.MASK_DOCUMENT, I.MASK_DOCUMENT_BIDIR])
+def test_d64_document_key_tile_edges(mask, lens):
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    w = I.document_workload(800 + len(lens), int(cu[-1]), 4, 64, cu_seqlens=cu, Hkv=1,
+                            mask_kind=mask)
+    compare(w, run(w), strict=False)
+
+
 @pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("W", [1, 2, 127, 128, 129, 300, 1000])
 def test_sliding_ragged(d, W):
