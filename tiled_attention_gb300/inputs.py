@@ -392,6 +392,10 @@ def config(k) -> Workload:
     if k == "5p16":
         return paged_decode_workload(1005, 32, 1024, 16384, 32, 8, 128, page_size=16, name=(
             "paged decode B32 L U[1024,16384] Hq32 Hkv8 d128 page16"))
+    # The headline causal shape at head dim 64 (long sequences: the d = 64 kernel's steady state).
+    if k == "3c64":
+        return dense_workload(1003, 2, 32, 8, 8192, 64, MASK_CAUSAL,
+                              name="causal B2 Hq32 Hkv8 N8192 d64")
     if k == "4b":
         return document_workload(1004, 16384, 16, 64, 256, 4096, mask_kind=MASK_DOCUMENT_BIDIR,
                                  name="non-causal document T16384 H16 d64 seg U[256,4096]")
