@@ -322,8 +322,9 @@ def test_paged_prefill_chunk_longer_than_context_reports_status():
     assert attn.attn_get_status() == attn.ATTN_ERR_SEQLENS
 
 
-def test_dense_decode_empty_context():
-    w = I.dense_decode_workload(9, 3, 0, 0, 8, 2, 128, N=100, context_lens=[0, 70, 0])
+@pytest.mark.parametrize("group", [1, 3, 4, 12])
+def test_dense_decode_empty_context(group):
+    w = I.dense_decode_workload(9, 3, 0, 0, 2 * group, 2, 128, N=100, context_lens=[0, 70, 0])
     dp = run(w)
     o, lse = dp.outputs()
     ro, rl = oracle.attention(w)
@@ -368,8 +369,9 @@ def test_dense_decode_length_past_cache_reports_status():
     assert attn.attn_get_status() == attn.ATTN_ERR_SEQLENS
 
 
-def test_paged_empty_context():
-    w = I.paged_decode_workload(9, 3, 0, 0, 8, 2, 128, context_lens=[0, 70, 0])
+@pytest.mark.parametrize("group", [1, 3, 4, 12])
+def test_paged_empty_context(group):
+    w = I.paged_decode_workload(9, 3, 0, 0, 2 * group, 2, 128, context_lens=[0, 70, 0])
     dp = run(w)
     o, lse = dp.outputs()
     ro, rl = oracle.attention(w)

@@ -292,21 +292,24 @@ __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
 // buffers): loads overlap the reduction and the conversion instead of following them.
 constexpr int kQuantThreads = 256;
 constexpr int kQuantBufBytes = kFp8Block * 128 * 2;  // one block: 128 rows x d <= 128 bf16
-constexpr int kQuantSmemBytes = 2 * kQuantBufBytes + 64;
+// Measured on GB300 (Q and K of the causal N=8192 workload, 251 MB): three CTAs per SM with
+// two buffers each, 54 us; two CTAs with three buffers, 60 us; 512 threads per CTA, 58 us.
+constexpr int kQuantBufs = 2;  // blocks in flight or in use per CTA
+constexpr int kQuantCtasPerSm = 3;
+constexpr int kQuantSmemBytes = kQuantBufs * kQuantBufBytes + 64;
 
 __global__ void __launch_bounds__(kQuantThreads)
     quantize_fp8_kernel(const uint8_t* __restrict__ x, uint2* __restrict__ x8,
                         float* __restrict__ scales, int N, int d, int nb, int nblocks,
                         int* status, unsigned long long timeout_ns) {
   extern __shared__ __align__(128) uint8_t qsm[];
-  uint64_t* bar = reinterpret_cast<uint64_t*>(qsm + 2 * kQuantBufBytes);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(qsm + kQuantBufs * kQuantBufBytes);
   __shared__ float red[kQuantThreads / 32];
   __shared__ float s_scale;
   __shared__ int s_abort;
   const int tid = static_cast<int>(threadIdx.x);
   if (tid == 0) {
-    mbar_init(&bar[0], 1);
-    mbar_init(&bar[1], 1);
+    for (int b = 0; b < kQuantBufs; ++b) mbar_init(&bar[b], 1);
     s_abort = 0;
     fence_mbar_init();
   }
@@ -323,19 +326,22 @@ __global__ void __launch_bounds__(kQuantThreads)
   const int G = static_cast<int>(gridDim.x);
   int t = static_cast<int>(blockIdx.x);
   int issued = 0;  // copies issued by thread 0
-  if (tid == 0 && t < nblocks) {
-    issue(t, 0);
-    issued = 1;
-  }
-  int k = 0;
-  for (; t < nblocks; t += G, ++k) {
-    const int slot = k & 1;
-    // The other buffer was last read in the previous iteration, before its closing barrier.
-    if (tid == 0 && t + G < nblocks) {
-      issue(t + G, slot ^ 1);
+  if (tid == 0)
+    for (int j = 0; j < kQuantBufs - 1 && t + j * G < nblocks; ++j) {
+      issue(t + j * G, j);
       ++issued;
     }
-    const bool ok = mbar_wait(&bar[slot], (k >> 1) & 1, wc);
+  int k = 0;
+  for (; t < nblocks; t += G, ++k) {
+    const int slot = k % kQuantBufs;
+    // The buffer of the block kQuantBufs - 1 ahead was last read in the previous iteration,
+    // before its closing barrier.
+    const int ta = t + (kQuantBufs - 1) * G;
+    if (tid == 0 && ta < nblocks) {
+      issue(ta, (k + kQuantBufs - 1) % kQuantBufs);
+      ++issued;
+    }
+    const bool ok = mbar_wait(&bar[slot], (k / kQuantBufs) & 1, wc);
     if (!__syncthreads_and(ok)) break;
     const int pl = t / nb, bt = t % nb, r0 = bt * kFp8Block;
     const int nvec = imin(kFp8Block, N - r0) * d / 8;  // 8-element vectors of the block
@@ -394,7 +400,8 @@ __global__ void __launch_bounds__(kQuantThreads)
   }
   // After a timeout, let copies still in flight land before the CTA exits.
   if (tid == 0)
-    for (int j = k; j < issued; ++j) mbar_wait(&bar[j & 1], (j >> 1) & 1, wc_drain);
+    for (int j = k; j < issued; ++j)
+      mbar_wait(&bar[j % kQuantBufs], (j / kQuantBufs) & 1, wc_drain);
 }
 
 // Self-test of the bounded pipeline wait: one thread waits on an mbarrier that nothing
@@ -702,7 +709,7 @@ int attn_quantize_fp8(const void* x, void* x8, float* scales, int planes, int N,
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(quantize_fp8_kernel),
                                    kQuantSmemBytes, &done);
   if (e != cudaSuccess) return cuda_fail(e, "quantize smem attribute");
-  const int grid = nblocks < 3 * sms ? nblocks : 3 * sms;  // three CTAs per SM
+  const int grid = nblocks < kQuantCtasPerSm * sms ? nblocks : kQuantCtasPerSm * sms;
   quantize_fp8_kernel<<<grid, kQuantThreads, kQuantSmemBytes, static_cast<cudaStream_t>(stream)>>>(
       static_cast<const uint8_t*>(x), static_cast<uint2*>(x8), scales, N, d, nb, nblocks, status,
       kTimeoutNs);
