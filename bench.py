@@ -310,7 +310,7 @@ def suite(args):
             line.update(extra)
         print(json.dumps(line), flush=True)
 
-    for cfg in (1, 2, 3, "3c", "3c64", 4, "3b", "3p", "4b", "6", "6p64", 5, "5p16"):
+    for cfg in (1, 2, 3, "3c", "3c64", 4, "3b", "3p", "4b", "6", "6p64", 5, "5p16", "5b1", "5b4"):
         if wanted is not None and str(cfg) not in wanted:
             continue
         w = I.config(cfg)

@@ -389,6 +389,13 @@ def config(k) -> Workload:
                                       page_size=ps, name=(
                                           "chunked prefill B16 Lk U[2048,16384] Lq U[256,2048] "
                                           f"Hq32 Hkv8 d128 page{ps}"))
+    # Small batches of the paged decode: one 16K-token sequence, and four sequences of 1K-16K.
+    if k == "5b1":
+        return paged_decode_workload(1051, 1, 16384, 16384, 32, 8, 128, name=(
+            "paged decode B1 L16384 Hq32 Hkv8 d128 page64"))
+    if k == "5b4":
+        return paged_decode_workload(1054, 4, 1024, 16384, 32, 8, 128, name=(
+            "paged decode B4 L U[1024,16384] Hq32 Hkv8 d128 page64"))
     if k == "5p16":
         return paged_decode_workload(1005, 32, 1024, 16384, 32, 8, 128, page_size=16, name=(
             "paged decode B32 L U[1024,16384] Hq32 Hkv8 d128 page16"))
