@@ -397,6 +397,27 @@ def test_paged_empty_context(group):
     assert np.abs(lse[live] - rl[live]).max() <= LSE_TOL
 
 
+@pytest.mark.parametrize("fill", ["ones", "random"])
+def test_decode_workspace_needs_no_clearing(fill):
+    """The split tickets carry a per-call generation: a workspace holding anything (all-ones
+    bytes, random bytes) gives the oracle's results, and so does the next call on it."""
+    lens = [5000, 70, 16384, 1]
+    w = I.paged_decode_workload(23, len(lens), 0, 0, 24, 4, 128, context_lens=lens)
+    dp = DeviceProblem(w)
+    if fill == "ones":
+        dp.workspace.fill_(255)
+    else:
+        g = torch.Generator(device="cuda").manual_seed(5)
+        dp.workspace.copy_(torch.randint(0, 256, dp.workspace.shape, generator=g,
+                                         device="cuda", dtype=torch.int32).to(torch.uint8))
+    for _ in range(2):
+        dp.o.fill_(float("nan"))
+        assert dp.run() == 0, attn.last_error()
+        torch.cuda.synchronize()
+        assert attn.attn_get_status() == 0
+        compare(w, dp)
+
+
 # ------------------------------------------------------------------ bit-exact properties
 
 def test_gather_pages_bit_exact():
@@ -649,3 +670,13 @@ def test_cuda_graph_capture_and_replay():
     assert attn.attn_get_status() == 0
     compare(wp2, pp, strict=False)
     compare(wd2, pd)
+    # A second replay on other queries: the decode's split tickets, left cleared by the first
+    # replay, serve the replayed (same) generation again.
+    wd3 = I.paged_decode_workload(72, 3, 100, 2000, 8, 2, 128)
+    wd3.q = I.dense_workload(75, 3, 8, 2, 1, 128).q
+    pd.q.copy_(bf16_tensor(wd3.q, pd.q.device).reshape(pd.q.shape))
+    pd.o.fill_(float("nan"))
+    g.replay()
+    torch.cuda.synchronize()
+    assert attn.attn_get_status() == 0
+    compare(wd3, pd)
