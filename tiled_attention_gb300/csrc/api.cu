@@ -346,14 +346,16 @@ __global__ void __launch_bounds__(kQuantThreads)
     const int pl = t / nb, bt = t % nb, r0 = bt * kFp8Block;
     const int nvec = imin(kFp8Block, N - r0) * d / 8;  // 8-element vectors of the block
     const uint4* v = reinterpret_cast<const uint4*>(qsm + slot * kQuantBufBytes);
-    float amax = 0.f;
+    // Block maximum of |x| on packed bf16 pairs (abs and max are exact in bf16).
+    __nv_bfloat162 amax2 = __floats2bfloat162_rn(0.f, 0.f);
     for (int i = tid; i < nvec; i += kQuantThreads) {
       const uint4 q = v[i];
       const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
       for (int e = 0; e < 4; ++e)
-        amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(w[e])), fabsf(bf16_hi(w[e]))));
+        amax2 = __hmax2(amax2, __habs2(*reinterpret_cast<const __nv_bfloat162*>(&w[e])));
     }
+    float amax = fmaxf(__low2float(amax2), __high2float(amax2));
     for (int off = 16; off; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
     if ((tid & 31) == 0) red[tid >> 5] = amax;
     __syncthreads();
@@ -371,18 +373,20 @@ __global__ void __launch_bounds__(kQuantThreads)
     if (sc == 0.f) {
       for (int i = tid; i < nvec; i += kQuantThreads) out[i] = make_uint2(0u, 0u);
     } else if (isfinite(rc)) {
-      // Markstein's correction (see above); a zero quotient keeps the sign of the product.
-      auto quot = [&](float xv) {
-        const float q = xv * rc;
-        const float q1 = __fmaf_rn(__fmaf_rn(-q, sc, xv), rc, q);
-        return q1 == 0.f ? q : q1;
-      };
+      // Markstein's correction (see above) on pairs: one packed multiply and two packed
+      // FMAs per two elements; a zero quotient keeps the sign of the product.
+      const float2 rc2 = make_float2(rc, rc), nsc2 = make_float2(-sc, -sc);
       for (int i = tid; i < nvec; i += kQuantThreads) {
         const uint4 q = v[i];
         const uint32_t w[4] = {q.x, q.y, q.z, q.w};
         uint32_t c[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) c[e] = e4m3x2(quot(bf16_lo(w[e])), quot(bf16_hi(w[e])));
+        for (int e = 0; e < 4; ++e) {
+          const float2 xv = make_float2(bf16_lo(w[e]), bf16_hi(w[e]));
+          const float2 q0 = __fmul2_rn(xv, rc2);
+          const float2 q1 = __ffma2_rn(__ffma2_rn(q0, nsc2, xv), rc2, q0);
+          c[e] = e4m3x2(q1.x == 0.f ? q0.x : q1.x, q1.y == 0.f ? q0.y : q1.y);
+        }
         out[i] = make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
       }
     } else {
