@@ -24,7 +24,7 @@
 //
 // Combine: each split writes its unnormalised O, max m and sum l (log2 units) to the
 // workspace; the last split to finish (atomic ticket per (b, g)) merges them in split order,
-// reading each split's (m, l) once into shared memory:
+// each thread loading a batch of splits at once for four columns of one head:
 //   M = max_c m_c,  L = sum_c l_c 2^(m_c - M),  O = sum_c O_c 2^(m_c - M) / L,
 //   LSE = (M + log2 L) ln 2
 // — the same rescaling identity as the online update, applied across splits. The order is
@@ -75,7 +75,7 @@ struct DecodeCfg {
   static constexpr int kOffMax = 256, kOffSum = 512, kMiscBytes = 768;
   static constexpr int kSmemBytes = 1024 + kRingBytes + kMiscBytes;
   static_assert(G >= 1 && G <= 16, "query heads per kv head");
-  static_assert(2 * G * D * 4 <= kRingBytes, "merge buffer reuses the ring");
+  static_assert(kWarps * G * D * 4 <= kRingBytes, "the warps' O rows reuse the ring");
 };
 
 struct DecodeCtrl {
@@ -105,10 +105,6 @@ __device__ __forceinline__ void ldmatrix_x4_trans(uint32_t (&r)[4], uint32_t sad
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
                : "r"(saddr));
-}
-
-__device__ __forceinline__ uint16_t bf16_bits(float x) {
-  return static_cast<uint16_t>(pack_bf16x2(x, 0.f) & 0xFFFFu);
 }
 
 // Byte offset of the 16-byte chunk holding columns [d0, d0 + 8) of `token` in a page that TMA
@@ -415,141 +411,128 @@ __global__ void __launch_bounds__(160, 2)
       o[nt][3] *= f_hi;
     }
   }
-  // Sum the warps' rescaled O in a fixed order (3 + 2 -> 1 + 0, then 1 -> 0), through the idle
-  // ring: [2 slots][16 rows][D] fp32.
+  // Each warp's rescaled rows of the group's heads go to the idle ring, [warp][G][D] fp32.
+  // After one barrier every consumer thread sums four columns of one head over the warps in a
+  // fixed order, (w0 + w2) + (w1 + w3), and writes them out: the result is bit-reproducible,
+  // and the partials leave as coalesced 16-byte stores from all four warps.
   float* buf = reinterpret_cast<float*>(ring);
 #pragma unroll
-  for (int half = C::kWarps / 2; half >= 1; half >>= 1) {
-    if (warp >= half && warp < 2 * half) {
-      float* dst = buf + (warp - half) * 16 * D;
-#pragma unroll
-      for (int nt = 0; nt < C::kNTiles; ++nt) {
-        *reinterpret_cast<float2*>(dst + r * D + nt * 8 + 2 * q) = make_float2(o[nt][0], o[nt][1]);
-        *reinterpret_cast<float2*>(dst + (r + 8) * D + nt * 8 + 2 * q) =
-            make_float2(o[nt][2], o[nt][3]);
-      }
-    }
-    named_barrier_sync(1, C::kConsumers);
-    if (warp < half) {
-      const float* src = buf + warp * 16 * D;
-#pragma unroll
-      for (int nt = 0; nt < C::kNTiles; ++nt) {
-        const float2 lo = *reinterpret_cast<const float2*>(src + r * D + nt * 8 + 2 * q);
-        const float2 hi = *reinterpret_cast<const float2*>(src + (r + 8) * D + nt * 8 + 2 * q);
-        o[nt][0] += lo.x;
-        o[nt][1] += lo.y;
-        o[nt][2] += hi.x;
-        o[nt][3] += hi.y;
-      }
-    }
-    named_barrier_sync(1, C::kConsumers);
+  for (int nt = 0; nt < C::kNTiles; ++nt) {
+    if (r < G)
+      *reinterpret_cast<float2*>(buf + (warp * G + r) * D + nt * 8 + 2 * q) =
+          make_float2(o[nt][0], o[nt][1]);
+    if (C::kHi && r + 8 < G)
+      *reinterpret_cast<float2*>(buf + (warp * G + r + 8) * D + nt * 8 + 2 * q) =
+          make_float2(o[nt][2], o[nt][3]);
   }
+  named_barrier_sync(1, C::kConsumers);
 
   const size_t bg = static_cast<size_t>(b) * p.Hkv + g;
   const bool single = nsplit == 1;
-  if (warp == 0) {
-    float L_lo = 0.f, L_hi = 0.f;
+  constexpr int kQuads = D / 4;  // four-column groups of one head's row
+  for (int idx = tid; idx < G * kQuads; idx += C::kConsumers) {
+    const int hh = idx / kQuads, d0 = (idx % kQuads) * 4;
+    float4 w[C::kWarps];
 #pragma unroll
-    for (int w = 0; w < C::kWarps; ++w) {
-      const float mw_lo = red_m[w * 16 + r], mw_hi = red_m[w * 16 + r + 8];
-      if (mw_lo != -INFINITY) L_lo += red_l[w * 16 + r] * fast_exp2(mw_lo - M_lo);
-      if (mw_hi != -INFINITY) L_hi += red_l[w * 16 + r + 8] * fast_exp2(mw_hi - M_hi);
+    for (int ww = 0; ww < C::kWarps; ++ww)
+      w[ww] = *reinterpret_cast<const float4*>(buf + (ww * G + hh) * D + d0);
+    const float4 s = make_float4((w[0].x + w[2].x) + (w[1].x + w[3].x),
+                                 (w[0].y + w[2].y) + (w[1].y + w[3].y),
+                                 (w[0].z + w[2].z) + (w[1].z + w[3].z),
+                                 (w[0].w + w[2].w) + (w[1].w + w[3].w));
+    // The head's max and sum over the warps (the same M that rescaled each warp's O above).
+    float Mr = red_m[hh];
+#pragma unroll
+    for (int ww = 1; ww < C::kWarps; ++ww) Mr = fmaxf(Mr, red_m[ww * 16 + hh]);
+    float Lr = 0.f;
+#pragma unroll
+    for (int ww = 0; ww < C::kWarps; ++ww) {
+      const float mw = red_m[ww * 16 + hh];
+      if (mw != -INFINITY) Lr += red_l[ww * 16 + hh] * fast_exp2(mw - Mr);
     }
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      const int row = r + 8 * half;
-      if (row >= G) continue;
-      const float Lr = half ? L_hi : L_lo;
-      const float Mr = half ? M_hi : M_lo;
-      const size_t orow = head0 + row;
-      if (single) {
-        const float inv = Lr > 0.f ? 1.f / Lr : 0.f;
-        uint32_t* o32 = reinterpret_cast<uint32_t*>(o16 + orow * D);
-#pragma unroll
-        for (int nt = 0; nt < C::kNTiles; ++nt)
-          o32[nt * 4 + q] = pack_bf16x2(o[nt][2 * half] * inv, o[nt][2 * half + 1] * inv);
-        if (q == 0)
-          p.lse[orow] = Lr > 0.f ? (Mr + log2f(Lr)) * 0.69314718055994530942f : -INFINITY;
-      } else {
-        const size_t base = (bg * p.max_splits + split) * G + row;
-#pragma unroll
-        for (int nt = 0; nt < C::kNTiles; ++nt)
-          *reinterpret_cast<float2*>(p.part_o + base * D + nt * 8 + 2 * q) =
-              make_float2(o[nt][2 * half], o[nt][2 * half + 1]);
-        if (q == 0) {
-          p.part_ml[2 * base] = Mr;
-          p.part_ml[2 * base + 1] = Lr;
-        }
+    const size_t orow = head0 + hh;
+    if (single) {
+      const float inv = Lr > 0.f ? 1.f / Lr : 0.f;
+      *reinterpret_cast<uint2*>(o16 + orow * D + d0) =
+          make_uint2(pack_bf16x2(s.x * inv, s.y * inv), pack_bf16x2(s.z * inv, s.w * inv));
+      if (d0 == 0)
+        p.lse[orow] = Lr > 0.f ? (Mr + log2f(Lr)) * 0.69314718055994530942f : -INFINITY;
+    } else {
+      const size_t base = (bg * p.max_splits + split) * G + hh;
+      *reinterpret_cast<float4*>(p.part_o + base * D + d0) = s;
+      if (d0 == 0) {
+        p.part_ml[2 * base] = Mr;
+        p.part_ml[2 * base + 1] = Lr;
       }
     }
   }
   if (single) return;
 
-  __threadfence();
+  // Ticket: once every consumer has written its partials, thread 0 publishes them (a fence,
+  // then the counter) and the split that draws the last ticket merges.
   named_barrier_sync(1, C::kConsumers);
   if (tid == 0) {
+    __threadfence();
     const int ticket = atomicAdd(&p.counters[bg], 1);
+    __threadfence();
     ctl->is_last = ticket == nsplit - 1;
   }
   named_barrier_sync(1, C::kConsumers);
   if (!ctl->is_last) return;
   __threadfence();
-  // Last split of (b, g): merge the splits in split order. Every split's (m, l) is read once
-  // into shared memory (the ring is idle now) and turned into its weight 2^(m - M); each
-  // output element then sums its splits from independent loads, in split order, so the
-  // result is the same as a plain loop over the splits.
+  // Last split of (b, g): merge the splits in split order,
+  //   M = max_c m_c,  L = sum_c l_c 2^(m_c - M),  O = sum_c O_c 2^(m_c - M) / L,
+  // summing in split order as a plain loop over the splits would. Each thread takes four
+  // columns of one head and issues the loads of a whole batch of splits before it uses any,
+  // so the merge costs a few L2 round trips instead of one or more per split.
+  constexpr int kBatch = 16;
   const size_t base_bg = bg * p.max_splits * G;  // (b, g)'s first partial row
-  constexpr int kMergeCap = C::kRingBytes / (8 * GT);  // splits whose (w, l) fit the ring
-  if (nsplit <= kMergeCap) {
-    float* sw = reinterpret_cast<float*>(ring);  // [G][nsplit]: m, then the weight
-    float* sl = sw + G * nsplit;                 // [G][nsplit]: l
-    for (int hh = warp; hh < G; hh += C::kWarps) {
-      float M = -INFINITY;
-      for (int s = lane; s < nsplit; s += 32) {
-        const size_t bs = base_bg + static_cast<size_t>(s) * G + hh;
-        const float m = __ldcg(p.part_ml + 2 * bs);
-        sw[hh * nsplit + s] = m;
-        sl[hh * nsplit + s] = __ldcg(p.part_ml + 2 * bs + 1);
-        M = fmaxf(M, m);
+  for (int idx = tid; idx < G * kQuads; idx += C::kConsumers) {
+    const int hh = idx / kQuads, d0 = (idx % kQuads) * 4;
+    const float* ml = p.part_ml + 2 * (base_bg + hh);     // split c at + 2 c G
+    const float* po = p.part_o + (base_bg + hh) * D + d0;  // split c at + c G D
+    // M first, in its own pass, unless one batch holds every split.
+    float M = -INFINITY;
+    for (int c0 = 0; nsplit > kBatch && c0 < nsplit; c0 += kBatch) {
+      float mv[kBatch];
+#pragma unroll
+      for (int t = 0; t < kBatch; ++t)
+        mv[t] = c0 + t < nsplit ? __ldcg(ml + 2 * static_cast<size_t>(c0 + t) * G) : -INFINITY;
+#pragma unroll
+      for (int t = 0; t < kBatch; ++t) M = fmaxf(M, mv[t]);
+    }
+    float Ls = 0.f;
+    float4 Os = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int c0 = 0; c0 < nsplit; c0 += kBatch) {
+      float2 mlv[kBatch];
+      float4 ov[kBatch];
+#pragma unroll
+      for (int t = 0; t < kBatch; ++t) {
+        const size_t c = static_cast<size_t>(imin(c0 + t, nsplit - 1));
+        mlv[t] = __ldcg(reinterpret_cast<const float2*>(ml + 2 * c * G));
+        ov[t] = __ldcg(reinterpret_cast<const float4*>(po + c * G * D));
       }
-      for (int off = 16; off; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-      for (int s = lane; s < nsplit; s += 32) sw[hh * nsplit + s] = exp2f(sw[hh * nsplit + s] - M);
-      if (lane == 0) red_m[hh] = M;
-    }
-    named_barrier_sync(1, C::kConsumers);
-    if (tid < G) {
-      float Ls = 0.f;
-      for (int s = 0; s < nsplit; ++s) Ls += sl[tid * nsplit + s] * sw[tid * nsplit + s];
-      red_l[tid] = Ls;
-    }
-    named_barrier_sync(1, C::kConsumers);
-    for (int idx = tid; idx < G * D; idx += C::kConsumers) {
-      const int hh = idx / D, d = idx % D;
-      const float* wv = sw + hh * nsplit;
-      const float* po = p.part_o + (base_bg + hh) * D + d;
-      float Os = 0.f;
-#pragma unroll 4
-      for (int s = 0; s < nsplit; ++s) Os += __ldcg(po + static_cast<size_t>(s) * G * D) * wv[s];
-      const float Ls = red_l[hh];
-      o16[(head0 + hh) * D + d] = bf16_bits(Os / Ls);
-      if (d == 0) p.lse[head0 + hh] = (red_m[hh] + log2f(Ls)) * 0.69314718055994530942f;
-    }
-  } else {
-    for (int idx = tid; idx < G * D; idx += C::kConsumers) {
-      const int hh = idx / D, d = idx % D;
-      const size_t base0 = base_bg + hh;
-      float M = -INFINITY;
-      for (int s = 0; s < nsplit; ++s) M = fmaxf(M, __ldcg(p.part_ml + 2 * (base0 + s * G)));
-      float Ls = 0.f, Os = 0.f;
-      for (int s = 0; s < nsplit; ++s) {
-        const size_t bs = base0 + static_cast<size_t>(s) * G;
-        const float w = exp2f(__ldcg(p.part_ml + 2 * bs) - M);
-        Ls += __ldcg(p.part_ml + 2 * bs + 1) * w;
-        Os += __ldcg(p.part_o + bs * D + d) * w;
+      if (nsplit <= kBatch) {
+#pragma unroll
+        for (int t = 0; t < kBatch; ++t)
+          if (t < nsplit) M = fmaxf(M, mlv[t].x);
       }
-      o16[(head0 + hh) * D + d] = bf16_bits(Os / Ls);
-      if (d == 0) p.lse[head0 + hh] = (M + log2f(Ls)) * 0.69314718055994530942f;
+#pragma unroll
+      for (int t = 0; t < kBatch; ++t) {
+        if (c0 + t < nsplit) {
+          const float wt = exp2f(mlv[t].x - M);
+          Ls += mlv[t].y * wt;
+          Os.x += ov[t].x * wt;
+          Os.y += ov[t].y * wt;
+          Os.z += ov[t].z * wt;
+          Os.w += ov[t].w * wt;
+        }
+      }
     }
+    const size_t orow = head0 + hh;
+    *reinterpret_cast<uint2*>(o16 + orow * D + d0) =
+        make_uint2(pack_bf16x2(Os.x / Ls, Os.y / Ls), pack_bf16x2(Os.z / Ls, Os.w / Ls));
+    if (d0 == 0) p.lse[orow] = (M + log2f(Ls)) * 0.69314718055994530942f;
   }
   if (tid == 0) p.counters[bg] = 0;
 }
