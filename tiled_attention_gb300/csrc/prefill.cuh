@@ -24,6 +24,8 @@
 //               K_j, V_j into a STAGES-deep smem ring.
 //   warp 1      MMA issuer (one elected lane) and TMEM owner: S_i = Q_i K_j^T (SS MMA) and
 //               O_i += P_i V_j (P read from TMEM, V from smem).
+//   warp 3      paged prefill with pages under 64 tokens only: issues the V_j entries of the
+//               ring (warp 0 then issues the Q tiles and the K_j entries).
 //   warps 4-7   softmax warpgroup for query tile 0; warps 8-11 for query tile 1. One thread
 //               owns one query row (TMEM lane): it reads its S row, applies the element mask
 //               on boundary tiles only, updates m and l with exp2, writes P (bf16) back into
@@ -467,7 +469,14 @@ __global__ void __launch_bounds__(384, 1)
 
   if (warp < 4) {
     regs_decrease<C::kRegsControl>();
-    if (warp == 0) {
+    // Paged prefill with pages of 16 or 32 tokens: a key tile is 8 or 4 page boxes per 64-column
+    // panel, and one warp issues them more slowly than the tensor core consumes them (a clock64
+    // trace put the producer at ~1350 cycles per ring entry against ~750 with 64-token pages). So
+    // warp 3, idle otherwise, issues the V entries and warp 0 the Q loads and the K entries.
+    // (Written as one comparison with the warp index: the plain "warp == 0 || ..." form, though
+    // it reduces to "warp == 0" for the other kinds, changed ptxas's spills in their kernels.)
+    const bool split_v = MASK == kMaskPagedPrefill && p.page_shift < 6;
+    if (warp == (split_v && warp == 3 ? 3 : 0)) {
       // -------------------------------------------------------------- TMA producer
       int e = 0;   // K/V ring entries issued
       int qn = 0;  // Q loads issued
@@ -482,7 +491,7 @@ __global__ void __launch_bounds__(384, 1)
         geometry(un, rng, lo, hi);
         const int e1 = kRot ? extra_of(rng) : 0;
         if (lane == 0) {
-          for (int i = 0; i < 2 && ok; ++i) {
+          for (int i = 0; i < 2 && ok && (!split_v || warp == 0); ++i) {
             if (rng[i].hi <= rng[i].lo) continue;
             const int qb = qn % QB;
             ok = mbar_wait(&ctl->q_empty[qb], ((qn / QB) & 1) ^ 1, wc);
@@ -538,6 +547,7 @@ __global__ void __launch_bounds__(384, 1)
           int pl_next = hi > lo ? plane_of(kv_at(0, lo, hi, e1)) : 0;
           int pl = 0;
           for (int x = 0; x < 2 * (hi - lo) && ok; ++x, ++e) {
+            if (split_v && (x & 1) != (warp == 3 ? 1 : 0)) continue;  // the other warp's entry
             const int st = e % STAGES;
             if (lane == 0) ok = mbar_wait(&ctl->kv_empty[st], ((e / STAGES) & 1) ^ 1, wc);
             ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -546,13 +556,13 @@ __global__ void __launch_bounds__(384, 1)
             __syncwarp();
             const CUtensorMap* m = (x & 1) ? &tm_v : &tm_k;
             uint8_t* dst = kv_s + st * C::kKVBytes;
-            if (!(x & 1)) pl = pl_next;
+            if (split_v || !(x & 1)) pl = pl_next;  // the first entry of its tile this warp issues
             if (lane < nb) {
               for (int c = 0; c < C::kPanels; ++c)
                 tma_load_3d(dst + c * C::kChunkBytes + (lane << lp) * 128, m, &ctl->kv_full[st],
                             c * 64, 0, pl);
             }
-            if (!(x & 1) && x / 2 + 1 < hi - lo)
+            if ((split_v || !(x & 1)) && x / 2 + 1 < hi - lo)
               pl_next = plane_of(kv_at(x / 2 + 1, lo, hi, e1));
           }
         }
