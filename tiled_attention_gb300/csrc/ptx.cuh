@@ -194,6 +194,60 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
       : "memory");
 }
 
+// Eight SS MMAs of one accumulator chain from one elected lane: K = 8 steps of 16 columns of
+// two K-major operands stored as 64-column 128-byte-swizzle panels kP16 x 16 bytes apart (a step
+// is 32 bytes inside a panel row); the first step overwrites D.
+template <uint32_t kP16>
+__device__ __forceinline__ void mma_ss_chain8(uint32_t d_tmem, uint64_t a, uint64_t b,
+                                              uint32_t idesc) {
+  asm volatile(
+      "{\n .reg .pred e, t, f;\n"
+      " .reg .b64 a1, b1, a2, b2, a3, b3, a4, b4, a5, b5, a6, b6, a7, b7;\n"
+      " setp.ne.b32 t, 1, 0;\n setp.ne.b32 f, 0, 0;\n"
+      " add.s64 a1, %1, 2;\n add.s64 b1, %2, 2;\n add.s64 a2, %1, 4;\n add.s64 b2, %2, 4;\n"
+      " add.s64 a3, %1, 6;\n add.s64 b3, %2, 6;\n add.s64 a4, %1, %4;\n add.s64 b4, %2, %4;\n"
+      " add.s64 a5, a4, 2;\n add.s64 b5, b4, 2;\n add.s64 a6, a4, 4;\n add.s64 b6, b4, 4;\n"
+      " add.s64 a7, a4, 6;\n add.s64 b7, b4, 6;\n"
+      " elect.sync _|e, 0xffffffff;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, f;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, t;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], a2, b2, %3, t;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], a3, b3, %3, t;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], a4, b4, %3, t;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], a5, b5, %3, t;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], a6, b6, %3, t;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], a7, b7, %3, t;\n}" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "l"(static_cast<uint64_t>(kP16))
+      : "memory");
+}
+
+// Eight TS MMAs of one accumulator chain from one elected lane: A from TMEM (8 columns per
+// 16-key step), B an MN-major operand whose 16-key steps are 2048 bytes apart; the first step
+// accumulates iff acc0 != 0.
+__device__ __forceinline__ void mma_ts_chain8(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
+                                              uint32_t idesc, uint32_t acc0) {
+  asm volatile(
+      "{\n .reg .pred e, t, p;\n .reg .b64 b1, b2, b3, b4, b5, b6, b7;\n"
+      " .reg .b32 a1, a2, a3, a4, a5, a6, a7;\n"
+      " setp.ne.b32 t, 1, 0;\n setp.ne.b32 p, %4, 0;\n"
+      " add.s32 a1, %1, 8;\n add.s32 a2, %1, 16;\n add.s32 a3, %1, 24;\n add.s32 a4, %1, 32;\n"
+      " add.s32 a5, %1, 40;\n add.s32 a6, %1, 48;\n add.s32 a7, %1, 56;\n"
+      " add.s64 b1, %2, 128;\n add.s64 b2, %2, 256;\n add.s64 b3, %2, 384;\n"
+      " add.s64 b4, %2, 512;\n add.s64 b5, %2, 640;\n add.s64 b6, %2, 768;\n"
+      " add.s64 b7, %2, 896;\n"
+      " elect.sync _|e, 0xffffffff;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %3, t;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [a2], b2, %3, t;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [a3], b3, %3, t;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [a4], b4, %3, t;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [a5], b5, %3, t;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [a6], b6, %3, t;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [a7], b7, %3, t;\n}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc0)
+      : "memory");
+}
+
 // Arrive (once) on `bar` when every tcgen05 operation the elected lane issued so far has
 // completed.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
