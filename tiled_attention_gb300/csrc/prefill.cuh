@@ -619,9 +619,15 @@ __global__ void __launch_bounds__(384, 1)
             return (kRot && i == 1) ? (j >= hi - e1 ? j - (hi - e1) : j - rlo + e1) : j - rlo;
           };
           auto key_at = [&](int x) { return kRot ? kv_at(x, lo, hi, e1) : lo + x; };
+          // Satisfied checks are tested once first and the bounded wait runs only when an
+          // entry is not there yet (as in the d = 128 issuer below): these warps share their
+          // sub-partitions with the softmax warps that bound d = 64. Measured on GB300: dense
+          // causal -1.5 %, non-causal document -3 %, no mask and sliding window -1.9 %.
           auto wait_entry = [&](int en) {
+            if (__all_sync(kFull, mbar_try_wait(&ctl->kv_full[en % STAGES], (en / STAGES) & 1)))
+              return true;
             return __all_sync(kFull,
-                              mbar_wait(&ctl->kv_full[en % STAGES], (en / STAGES) & 1, wc));
+                              mbar_wait(&ctl->kv_full[en % STAGES], (en / STAGES) & 1, wc)) != 0;
           };
           // S of position x (if this tile sees that key tile), then release K of x.
           auto do_k = [&](int x) -> bool {
@@ -658,7 +664,8 @@ __global__ void __launch_bounds__(384, 1)
             const int j = key_at(x);
             if (j >= rlo && j < rhi) {
               const int buf = pn & 1;
-              if (!__all_sync(kFull, mbar_wait(&ctl->p_ready2[i][buf], (pn >> 1) & 1, wc)))
+              if (!__all_sync(kFull, mbar_try_wait(&ctl->p_ready2[i][buf], (pn >> 1) & 1)) &&
+                  !__all_sync(kFull, mbar_wait(&ctl->p_ready2[i][buf], (pn >> 1) & 1, wc)))
                 return false;
               tc_fence_after();
               const int t = my_index(j);
