@@ -634,7 +634,7 @@ def _fuzz_workload(idx):
     return I.dense_workload(seed, B, Hq, Hkv, N, d, kind, window, name=f"fuzz{idx}")
 
 
-@pytest.mark.parametrize("idx", range(40))
+@pytest.mark.parametrize("idx", range(200))
 def test_randomized_shapes(idx):
     w = _fuzz_workload(idx)
     compare(w, run(w), strict=False)
