@@ -117,6 +117,28 @@ def test_fp8_attention_ragged(mask, window, N):
     compare(w, run(w), strict=False)
 
 
+_FP8_KINDS = [I.MASK_NONE, I.MASK_CAUSAL, I.MASK_SLIDING, I.MASK_SLIDING_BIDIR, I.MASK_PREFIX_LM]
+
+
+@pytest.mark.parametrize("idx", range(60))
+def test_fp8_randomized_shapes(idx):
+    """Case idx: its mask kind in turn; batch, GQA group, length (crossing 128-row tiles) and
+    window or prefix (also past the sequence) drawn from a generator seeded by idx."""
+    rng = np.random.default_rng(7000 + idx)
+    mask = _FP8_KINDS[idx % len(_FP8_KINDS)]
+    B = int(rng.integers(1, 4))
+    Hkv = int(rng.integers(1, 4))
+    Hq = Hkv * int(rng.integers(1, 5))
+    N = int(rng.integers(1, 1500))
+    window = 0
+    if mask == I.MASK_SLIDING:
+        window = int(rng.integers(1, N + 130))
+    elif mask in (I.MASK_SLIDING_BIDIR, I.MASK_PREFIX_LM):
+        window = int(rng.integers(0, N + 130))
+    w = fp8_workload(7000 + idx, B, Hq, Hkv, N, mask, window)
+    compare(w, run(w), strict=False)
+
+
 def test_fp8_zero_key_tile():
     """An all-zero key tile has scale 0: its scores are exactly 0 and masked keys stay
     masked (no NaN from 0 * -inf)."""
