@@ -399,8 +399,9 @@ def test_paged_empty_context(group):
 
 @pytest.mark.parametrize("fill", ["ones", "random"])
 def test_decode_workspace_needs_no_clearing(fill):
-    """The split tickets carry a per-call generation: a workspace holding anything (all-ones
-    bytes, random bytes) gives the oracle's results, and so does the next call on it."""
+    """The split tickets are zeroed on the call's stream before each launch: a workspace holding
+    anything (all-ones bytes, random bytes) gives the oracle's results, and so does the next
+    call on it."""
     lens = [5000, 70, 16384, 1]
     w = I.paged_decode_workload(23, len(lens), 0, 0, 24, 4, 128, context_lens=lens)
     dp = DeviceProblem(w)
@@ -416,6 +417,16 @@ def test_decode_workspace_needs_no_clearing(fill):
         torch.cuda.synchronize()
         assert attn.attn_get_status() == 0
         compare(w, dp)
+
+
+@pytest.mark.parametrize("d,Hq", [(128, 8), (64, 32)])
+def test_paged_decode_many_splits(d, Hq):
+    """Contexts of ~70K and ~20K tokens split into 69 and 20 splits of 1024 tokens: the last
+    split's merge runs its max pass and several batches of 16 splits; every row against the
+    oracle (groups of 4 and 16 query heads per kv head)."""
+    lens = [70000, 20001]
+    w = I.paged_decode_workload(31 + d, len(lens), 0, 0, Hq, 2, d, context_lens=lens)
+    compare(w, run(w))
 
 
 # ------------------------------------------------------------------ bit-exact properties
