@@ -206,9 +206,10 @@ int sms_or_default() {
 // but need enough (sequence, kv head) groups to fill the GPU. Measured on GB300: with 32
 // sequences x 8 kv heads of 1K-16K tokens, 32 stages run 3.5 % faster than 16 with 64-token
 // pages and 3.9 % with 16-token pages (48 and 64 are slower); with one 16K-token sequence x 8
-// kv heads, 16 stages take 32 us and 4 stages 65 us (a CTA of 4 stages barely fills its
-// ring). So: 32 once there are as many groups as SMs, else 16. The choice depends on B and
-// Hkv only, so every decode of the same batch shape splits, and rounds, the same way.
+// kv heads, 16 stages take 25.6 us, 8 stages 27.6 us and 4 stages 33.8 us, and splits sized to
+// cover all SMs (14 stages) change nothing. So: 32 once there are as many groups as SMs, else
+// 16. The choice depends on B and Hkv only, so every decode of the same batch shape splits,
+// and rounds, the same way.
 int decode_chunk_pages(int B, int Hkv) {
   return static_cast<long long>(B) * Hkv >= sms_or_default() ? 32 : 16;
 }

@@ -23,7 +23,9 @@
 //   warp 0      TMA producer: per unit, the two Q tiles into the next free Q buffers, then
 //               K_j, V_j into a STAGES-deep smem ring.
 //   warp 1      MMA issuer (one elected lane) and TMEM owner: S_i = Q_i K_j^T (SS MMA) and
-//               O_i += P_i V_j (P read from TMEM, V from smem).
+//               O_i += P_i V_j (P read from TMEM, V from smem). At d = 64 (96-key tiles, two
+//               S buffers per query tile) warp 1 issues query tile 0's MMAs and warp 2 tile
+//               1's.
 //   warp 3      paged prefill with pages under 64 tokens only: issues the V_j entries of the
 //               ring (warp 0 then issues the Q tiles and the K_j entries).
 //   warps 4-7   softmax warpgroup for query tile 0; warps 8-11 for query tile 1. One thread
@@ -31,9 +33,11 @@
 //               on boundary tiles only, updates m and l with exp2, writes P (bf16) back into
 //               TMEM over S, rescales its O row only when the max grew by more than 2^8, and
 //               finally writes O / l (bf16) and the LSE.
-// TMEM columns: S_0/P_0 [0,128), S_1/P_1 [128,256), O_0 [256,256+D), O_1 [256+D,256+2D).
+// TMEM columns at d = 128: S_0/P_0 [0,128), S_1/P_1 [128,256), O_0 [256,384), O_1 [384,512).
+// At d = 64: S/P buffer b of query tile i at [(2i + b) * 96, (2i + b + 1) * 96), O_0 and O_1 in
+// the 128 columns after the four buffers.
 //
-// Issue order per key tile j: PV_0(j-1), S_0(j), PV_1(j-1), S_1(j). tcgen05 MMAs of one
+// Issue order per key tile j at d = 128: PV_0(j-1), S_0(j), PV_1(j-1), S_1(j). tcgen05 MMAs of one
 // thread complete in order, so S_i(j) overwrites P_i(j-1) only after PV_i(j-1) has read it,
 // and "S_i(j) complete" implies "PV_i(j-1) complete": the softmax may rescale O_i right after
 // it sees S_i(j). While warpgroup 0 works on S_0(j), the tensor core runs PV_1 / S_1 and the
