@@ -230,8 +230,10 @@ int attn_gather_pages(const void *pool, void *dst, const int32_t *block_table, i
  *    (attn_noalloc_scratch_bytes()); nothing is launched then.
  *  - The first call on each device looks up the array's device address (cudaGetSymbolAddress)
  *    with that device current; make that first call before any stream capture.
- *  - Every call shares the one array per device and it keeps the last call's contents (the
- *    call zeroes what must start at zero on its stream). Calls whose kernels overlap on the
+ *  - Every call shares the one array per device and it keeps the last call's contents. Its
+ *    split tickets sit in a fixed region before the partials (one int per sequence x kv head,
+ *    B * Hkv at most 65536): zero when the library loads, and left zero by every launch that
+ *    runs to its end, so this entry point issues no memset. Calls whose kernels overlap on the
  *    GPU (different streams, or host threads without ordering) race on it: order them.
  */
 int attn_paged_decode_noalloc(const void *q, const void *k, const void *v, void *o, float *lse,
@@ -239,8 +241,9 @@ int attn_paged_decode_noalloc(const void *q, const void *k, const void *v, void 
                               const int32_t *cu_seqlens, const int32_t *block_table,
                               int page_size, int num_pages, void *stream);
 
-/* Size in bytes of attn_paged_decode_noalloc's fixed scratch array (16 MiB): a request is
- * served iff attn_workspace_bytes() of it, with mask_kind PAGED_DECODE, is at most this. */
+/* Size in bytes of attn_paged_decode_noalloc's scratch for partials (16 MiB; its 256 KiB of
+ * tickets come on top): a request is served iff attn_workspace_bytes() of it, with mask_kind
+ * PAGED_DECODE, is at most this. */
 size_t attn_noalloc_scratch_bytes(void);
 
 /* Synchronises `stream`, then returns and clears the device status word (ATTN_OK or one of

@@ -52,9 +52,15 @@ int g_num_sms[kMaxDevices];
 // Split-KV scratch of attn_paged_decode_noalloc, for callers that cannot allocate: one fixed
 // array per device, held from the library's load until the process exits. Its device address
 // is looked up once per device (cudaGetSymbolAddress) and cached here; attn_release forgets it
-// together with the status word's.
-constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;  // 16 MiB
-static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+// together with the status word's. The first kNoAllocTicketBytes hold the split tickets, one
+// int per (sequence, kv head): zero when the library loads (device globals start zeroed), and
+// every decode launch that runs to its end leaves them zero again, so this entry point needs
+// no memset. 65536 tickets cover every request whose partials fit the 16 MiB after them (at
+// least 268 bytes per group). The partials follow.
+constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;   // 16 MiB of partials
+constexpr size_t kNoAllocTicketBytes = size_t(256) << 10;   // 65536 tickets
+static __device__ __align__(256) unsigned char
+    g_noalloc_scratch[kNoAllocTicketBytes + kNoAllocScratchBytes];
 void* g_noalloc_scratch_ptr[kMaxDevices];
 
 int sm_count(int* out) {
@@ -488,11 +494,16 @@ size_t attn_workspace_bytes(int B, int Hq, int Hkv, int N, int d, int mask_kind,
   return decode_layout(B, Hq, Hkv, N, d).total;
 }
 
-int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+namespace ta {
+namespace {
+// The body of attn_fwd. `tickets`, when not null, is a ticket array that is already zero (the
+// allocation-free scratch's): the decode then uses it instead of the workspace's and skips
+// the memset that clears those.
+int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
              int Hkv, int N, int d, float scale, int mask_kind, int window,
              const int32_t* cu_seqlens, const int32_t* block_table, int page_size,
-             int num_pages, void* workspace, size_t workspace_bytes, void* stream_) {
-  g_last_error.clear();
+             int num_pages, void* workspace, size_t workspace_bytes, int* tickets,
+             void* stream_) {
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
   if (mask_kind < ATTN_MASK_NONE || mask_kind > ATTN_MASK_PREFIX_LM)
     return fail(ATTN_ERR_INVALID, "unknown mask_kind %d", mask_kind);
@@ -565,7 +576,7 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
     p.lse = lse;
     p.part_o = reinterpret_cast<float*>(ws + L.part_o);
     p.part_ml = reinterpret_cast<float*>(ws + L.part_ml);
-    p.counters = reinterpret_cast<int*>(ws + L.counters);
+    p.counters = tickets ? tickets : reinterpret_cast<int*>(ws + L.counters);
     p.B = B;
     p.Hq = Hq;
     p.Hkv = Hkv;
@@ -579,9 +590,11 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
     p.scale_log2 = scale * kLog2e;
     p.status = status;
     p.timeout_ns = kTimeoutNs;
-    cudaError_t e = cudaMemsetAsync(p.counters, 0, sizeof(int) * static_cast<size_t>(B) * Hkv,
-                                    stream);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(counters)");
+    cudaError_t e = cudaSuccess;
+    if (!tickets) {
+      e = cudaMemsetAsync(p.counters, 0, sizeof(int) * static_cast<size_t>(B) * Hkv, stream);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(counters)");
+    }
     e = launch_decode(d, group, tk, tv, p, dim3(L.max_splits, Hkv, B), stream);
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
     return ATTN_OK;
@@ -622,6 +635,17 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
                           : launch_prefill_d128(mask_kind, tq, tk, tv, to, p, grid, stream);
   if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
   return ATTN_OK;
+}
+}  // namespace
+}  // namespace ta
+
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+             int Hkv, int N, int d, float scale, int mask_kind, int window,
+             const int32_t* cu_seqlens, const int32_t* block_table, int page_size,
+             int num_pages, void* workspace, size_t workspace_bytes, void* stream) {
+  g_last_error.clear();
+  return fwd_impl(q, k, v, o, lse, B, Hq, Hkv, N, d, scale, mask_kind, window, cu_seqlens,
+                  block_table, page_size, num_pages, workspace, workspace_bytes, nullptr, stream);
 }
 
 int attn_fwd_paged_prefill(const void* q, const void* k, const void* v, void* o, float* lse,
@@ -984,12 +1008,16 @@ extern "C" int attn_paged_decode_noalloc(const void* q, const void* k, const voi
                 "this decode needs %zu bytes of split-KV scratch; the allocation-free entry "
                 "point has %zu (fewer sequences, kv heads or a shorter longest context fit)",
                 need, kNoAllocScratchBytes);
+  if (static_cast<long long>(B) * Hkv > static_cast<long long>(kNoAllocTicketBytes / sizeof(int)))
+    return fail(ATTN_ERR_UNSUPPORTED, "B * Hkv %lld above the %zu tickets of the scratch",
+                static_cast<long long>(B) * Hkv, kNoAllocTicketBytes / sizeof(int));
   void* scratch = nullptr;
   int rc = noalloc_scratch(&scratch);
   if (rc) return rc;
-  // The decode path zeroes the tickets it needs (cudaMemsetAsync, no allocation) on `stream`
-  // before its kernel; the partials are written before they are read.
-  return attn_fwd(q, k, v, o, lse, B, Hq, Hkv, N, d, scale, ATTN_MASK_PAGED_DECODE, 0,
-                  cu_seqlens, block_table, page_size, num_pages, scratch, kNoAllocScratchBytes,
-                  stream);
+  // The tickets are the scratch's fixed, already-zero ones (no memset); the partials, written
+  // before they are read, follow them.
+  uint8_t* base = static_cast<uint8_t*>(scratch);
+  return fwd_impl(q, k, v, o, lse, B, Hq, Hkv, N, d, scale, ATTN_MASK_PAGED_DECODE, 0,
+                  cu_seqlens, block_table, page_size, num_pages, base + kNoAllocTicketBytes,
+                  kNoAllocScratchBytes, reinterpret_cast<int*>(base), stream);
 }
