@@ -9,7 +9,8 @@ cudaMalloc / cudaFree imply is not allowed. attn_paged_decode_noalloc serves the
 Both entry points run the same kernel with the same split of the context and merge the splits
 in a fixed order, so their results must agree bit for bit: the GPU tests compare with
 torch.equal, on consecutive calls that reuse the array, on a small call right after a large
-one (which leaves stale partials and tickets behind), at the largest request the array holds,
+one (which leaves stale partials behind; the tickets, which this entry point never zeroes,
+must be back at zero), at the largest request the array holds,
 and after attn_release has made the library look the array's address up again. One case is
 also checked against the fp64 oracle. The CPU tests check that invalid arguments report their
 own reason and that the size limit falls exactly where attn_workspace_bytes puts it. This file
