@@ -316,6 +316,21 @@ def suite(args):
         w = I.config(cfg)
         dp = DeviceProblem(w, device=dev, fill_outputs=0.0)
         emit(w, timed(lambda: dp.run(stream), args.steps))
+        if cfg in ("5b1", "5b4"):
+            # The allocation-free entry point on the same inputs: its tickets live in a zeroed
+            # region of the library's scratch, so it issues no memset before the kernel.
+            o_na, lse_na = torch.empty_like(dp.o), torch.empty_like(dp.lse)
+
+            def noalloc():
+                return attn.attn_paged_decode_noalloc(dp.q, dp.k, dp.v, o_na, lse_na, w.B, w.Hq,
+                                                      w.Hkv, w.N, w.d, w.scale, dp.cu, dp.table,
+                                                      w.page_size, dp.num_pages, stream)
+
+            ms_na = timed(noalloc, args.steps)
+            same = (torch.equal(o_na.view(torch.int16), dp.o.view(torch.int16)) and
+                    torch.equal(lse_na, dp.lse))
+            emit(w, ms_na, {"workload": w.name + " (allocation-free entry point)",
+                            "bit_identical_to_attn_fwd": bool(same)})
         if cfg == 5:
             # Two-stage path of the paged-KV pattern: gather K and V pages into dense caches,
             # then the decode kernel reads the caches.
