@@ -429,6 +429,34 @@ def test_paged_decode_many_splits(d, Hq):
     compare(w, run(w))
 
 
+@pytest.mark.parametrize("idx", range(12))
+def test_paged_decode_randomized_long(idx):
+    """Batch, kv heads, group (1-16), head dim, page size and contexts of up to 40K tokens
+    (up to 40 splits per group, several merge batches) drawn from a generator seeded by idx;
+    every row against the oracle, and the allocation-free entry point bit-identical to
+    attn_fwd whenever its scratch holds the request."""
+    rng = np.random.default_rng(9000 + idx)
+    B, Hkv, G = int(rng.integers(1, 9)), int(rng.integers(1, 9)), int(rng.integers(1, 17))
+    d, page = int(rng.choice([64, 128])), int(rng.choice([16, 32, 64, 128]))
+    lens = rng.integers(0, 40001, B)
+    w = I.paged_decode_workload(9000 + idx, B, 0, 0, G * Hkv, Hkv, d, page_size=page,
+                                context_lens=lens, name=f"decode fuzz {idx}")
+    dp = run(w)
+    compare(w, dp, strict=False)
+    need = attn.attn_workspace_bytes(w.B, w.Hq, w.Hkv, w.N, w.d, w.mask_kind, w.page_size)
+    if need <= attn.attn_noalloc_scratch_bytes():
+        o = torch.full_like(dp.o, float("nan"))
+        lse = torch.full_like(dp.lse, float("nan"))
+        rc = attn.attn_paged_decode_noalloc(dp.q, dp.k, dp.v, o, lse, w.B, w.Hq, w.Hkv, w.N,
+                                            w.d, w.scale, dp.cu, dp.table, w.page_size,
+                                            dp.num_pages, None)
+        assert rc == 0, attn.last_error()
+        torch.cuda.synchronize()
+        assert attn.attn_get_status() == 0
+        assert torch.equal(o.view(torch.int16), dp.o.view(torch.int16))
+        assert torch.equal(lse, dp.lse)
+
+
 # ------------------------------------------------------------------ bit-exact properties
 
 def test_gather_pages_bit_exact():
