@@ -471,8 +471,18 @@ __global__ void __launch_bounds__(384, 1)
   // work, in tile order, so all roles agree on which buffer (count % QB) holds which tile.
   UnitCursor cur{0, 0, 0, 0};  // this role's place in the packed unit list
 
+  // Register split between warpgroup 0 and the softmax warpgroups. The window and prefix-LM
+  // kinds at d = 128 run faster with 96 / 200 (A/B on GB300: sliding window -1 %, two-sided
+  // -2.1 %, prefix-LM -3 %; 128*96 + 256*200 = 63488 of the 64512 launched); the other kinds
+  // keep 88 / 208 (headline unchanged, document d=64 and chunked prefill slower with 96 / 200).
+  constexpr bool kWideControl = D == 128 && !FP8 &&
+                                (MASK == kMaskSliding || MASK == kMaskSlidingBidir ||
+                                 MASK == kMaskPrefixLM);
+  constexpr uint32_t kRegsCtl = kWideControl ? 96 : C::kRegsControl;
+  constexpr uint32_t kRegsSm = kWideControl ? 200 : C::kRegsSoftmax;
+  static_assert(128 * kRegsCtl + 256 * kRegsSm <= 384 * 168, "register split above the launch");
   if (warp < 4) {
-    regs_decrease<C::kRegsControl>();
+    regs_decrease<kRegsCtl>();
     // Paged prefill with pages of 16 or 32 tokens: a key tile is 8 or 4 page boxes per 64-column
     // panel, and one warp issues them more slowly than the tensor core consumes them (a clock64
     // trace put the producer at ~1350 cycles per ring entry against ~750 with 64-token pages). So
@@ -826,7 +836,7 @@ __global__ void __launch_bounds__(384, 1)
       mbar_wait(&ctl->drain[warp - 1], 0, wc_drain);
     }
   } else {
-    regs_increase<C::kRegsSoftmax>();
+    regs_increase<kRegsSm>();
     // ---------------------------------------------------------------- softmax warpgroups
     const int i = (warp - 4) >> 2;          // query tile
     const int quarter = warp & 3;           // TMEM lanes [32*quarter, 32*quarter + 32)
