@@ -293,6 +293,8 @@ def pin_logit_shift(attn, kind):
     o1, l1 = attn(w1)
     s = float(np.float32(w0.scale))
     np.testing.assert_allclose(o1, o0, rtol=0, atol=1e-12)
+    # Every row of these cases sees at least one key, so both LSEs are finite.
+    assert np.isfinite(l0).all() and np.isfinite(l1).all()
     np.testing.assert_allclose(l1 - l0, 5.0 * s, rtol=0, atol=1e-12)
 
 
