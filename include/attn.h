@@ -221,9 +221,10 @@ int attn_gather_pages(const void *pool, void *dst, const int32_t *block_table, i
  *
  * Same arguments, layouts and results as attn_fwd with mask_kind = ATTN_MASK_PAGED_DECODE,
  * without the workspace: the split-KV scratch is a fixed 16 MiB (16777216-byte) array inside
- * the library, held by every GPU that loads it until the process exits. Meant for callers that get no scratch buffer from
- * their host framework (a custom-op interface, another framework's memory pool) or must not
- * let cudaMalloc / cudaFree synchronise the device on a serving path. It allocates nothing.
+ * the library, held by every GPU that loads it until the process exits. Meant for callers
+ * that get no scratch buffer from their host framework (a custom-op interface, another
+ * framework's memory pool) or must not let cudaMalloc / cudaFree synchronise the device on a
+ * serving path. It allocates nothing.
  *  - Arguments are checked first as attn_fwd checks them (ATTN_ERR_INVALID or
  *    ATTN_ERR_UNSUPPORTED with the reason). Then it returns ATTN_ERR_UNSUPPORTED, with a
  *    message, when attn_workspace_bytes() of the request exceeds the array
