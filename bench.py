@@ -49,17 +49,44 @@ def load_peaks():
                 "source": "fallback"}
 
 
+def code_tokens(src: str) -> str:
+    """C/C++/CUDA source with its comments removed and every run of whitespace made one space,
+    so that editing a comment or re-wrapping lines leaves the hash of a kernel unchanged.
+    String and character literals are kept as they are."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def kernel_source_hash(names):
+    """Hash of the code (not the comments) of the named files under csrc/."""
     h = hashlib.sha256()
     for n in names:
-        with open(os.path.join(ROOT, "tiled_attention_gb300", "csrc", n), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "tiled_attention_gb300", "csrc", n), encoding="utf-8") as f:
+            h.update(code_tokens(f.read()).encode())
     return h.hexdigest()[:16]
 
 
 def recorded_traffic(kernel: str, sources):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on this exact
-    kernel source; else None."""
+    kernel code (comments aside); else None."""
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
             rec = json.load(f).get(kernel)

@@ -61,23 +61,23 @@ def compare(w, dp, rows=None, strict=True):
 
 # ------------------------------------------------------------------ the five workloads
 
-def test_config1_dense():
+def test_dense_b1_h1_n256_d64():
     w = I.config(1)
     compare(w, run(w))
 
 
-def test_config2_causal():
+def test_causal_b4_h16_n2048_d128():
     w = I.config(2)
     compare(w, run(w))
 
 
-def test_config3_sliding_gqa():
+def test_sliding_w4096_b2_hq32_hkv8_n8192_d128():
     """Every one of the 524,288 output rows against the oracle."""
     w = I.config(3)
     compare(w, run(w))
 
 
-def test_config4_document():
+def test_document_t16384_h16_d64():
     w = I.config(4)
     compare(w, run(w))
 
@@ -98,7 +98,7 @@ def test_small_batch_paged_decode(cfg):
     assert torch.equal(dp.o.view(torch.int16), o1) and torch.equal(dp.lse, l1)
 
 
-def test_config5_paged_decode():
+def test_paged_decode_b32_hq32_hkv8_d128_page64():
     w = I.config(5)
     compare(w, run(w))
 

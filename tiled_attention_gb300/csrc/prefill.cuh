@@ -362,7 +362,7 @@ __global__ void __launch_bounds__(384, 1)
   // (boundary tiles at both edges of every row's range; sliding -4.8 %, two-sided -5.5 %)
   // and the document kinds at d = 64 (-4.3 %). The causal, prefix-LM and paged kinds keep
   // the compare-per-score form: with the other form their kernels compiled to a slower
-  // softmax overall (headline +6.9 %), though boundary tiles are 1.5 % of their tiles.
+  // softmax overall (causal N=8192 +6.9 %), though boundary tiles are 1.5 % of their tiles.
   constexpr bool kBitMask = MASK == kMaskSliding || MASK == kMaskSlidingBidir ||
                             (D == 64 && (MASK == kMaskDocument || MASK == kMaskDocumentBidir));
   static_assert(!FP8 || (D == 128 && !is_packed(MASK)), "FP8: dense kinds, D = 128");
@@ -474,7 +474,8 @@ __global__ void __launch_bounds__(384, 1)
   // Register split between warpgroup 0 and the softmax warpgroups. The window and prefix-LM
   // kinds at d = 128 run faster with 96 / 200 (A/B on GB300: sliding window -1 %, two-sided
   // -2.1 %, prefix-LM -3 %; 128*96 + 256*200 = 63488 of the 64512 launched); the other kinds
-  // keep 88 / 208 (headline unchanged, document d=64 and chunked prefill slower with 96 / 200).
+  // keep 88 / 208 (causal N=8192 unchanged, document d=64 and chunked prefill slower with
+  // 96 / 200).
   constexpr bool kWideControl = D == 128 && !FP8 &&
                                 (MASK == kMaskSliding || MASK == kMaskSlidingBidir ||
                                  MASK == kMaskPrefixLM);
@@ -739,7 +740,8 @@ __global__ void __launch_bounds__(384, 1)
           // on the critical path at d = 128: its satisfied barrier checks cost ~430 cycles per
           // step done one after the other. So V's and K's entries are tested together first
           // (two independent try_waits, one vote); the bounded waits run only if one is not
-          // ready. Measured on GB300: headline -3.5 %, sliding window -3.9 %, config 2 -2.8 %.
+          // ready. Measured on GB300: causal B2 Hq32 Hkv8 N8192 -3.5 %, sliding window -3.9 %,
+          // causal B4 H16 N2048 -2.8 %.
           {
             const bool rv = !have_v || mbar_try_wait(&ctl->kv_full[ev % STAGES], (ev / STAGES) & 1);
             const bool rk = !have_k || mbar_try_wait(&ctl->kv_full[ek % STAGES], (ek / STAGES) & 1);

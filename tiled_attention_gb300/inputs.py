@@ -373,8 +373,8 @@ def config(k) -> Workload:
         return paged_decode_workload(1005, 32, 1024, 16384, 32, 8, 128, name=(
             "paged decode B32 L U[1024,16384] Hq32 Hkv8 d128 page64"))
     # The mask variants on the same shapes: a two-sided window with as many keys per query as
-    # the causal window above, a prefix of half the sequence, and config 4's segments without
-    # the causal constraint.
+    # the causal window above, a prefix of half the sequence, and the 16384-token document
+    # packing's segments without the causal constraint.
     if k == "3b":
         return dense_workload(1003, 2, 32, 8, 8192, 128, MASK_SLIDING_BIDIR, window=2048,
                               name="two-sided window W2048 B2 Hq32 Hkv8 N8192 d128")
